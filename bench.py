@@ -1,0 +1,497 @@
+"""Benchmark of the fused GQA attention path on GB300.
+
+Headline (one JSON line on stdout, rank 0): single-token GQA decode at
+Qwen2.5-7B head geometry (B=1, Hq=28, Hkv=4, D=128), kv_len 32,768, fp32 KV
+cache, 28 layer calls on 28 distinct layer buffers per step.  Metric: decode
+K/V GB/s (algorithmic Q+K+V+O bytes / time), with its fraction of the measured
+HBM copy bandwidth.  The other rows of the hot path (the kv_len sweep in fp32
+and bf16, ragged batched decode, 4-bit decode, causal and chunked prefill) are
+measured in the same run and reported as sub-objects of the line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gqa|reference]
+
+Timing: CUDA events on the launching stream, W untimed warm-up steps, K timed
+steps bracketed by a barrier and a device synchronise; the inputs of one step
+(3.76 GB) are far larger than L2, so nothing is reused between steps.  For
+N > 1 (torchrun) every rank runs its own replica (weak scaling) and the time
+is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gqa_attention_kv_decode_gb300 import inputs, metrics  # noqa: E402
+
+HQ, HKV, D, LAYERS, S_HEAD = 28, 4, 128, 28, 32768
+METRIC = "GQA decode-attend KV GB/s (% of HBM peak); causal prefill TFLOP/s"
+WORKLOAD = ("single-token GQA decode, Qwen2.5-7B head geometry: B=1, Hq=28, Hkv=4, D=128, "
+            "kv_len=32768, fp32 KV cache, 28 layer calls on distinct buffers per step")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Dist:
+    """Barrier and max-over-ranks for replica timing (gloo, host-side only)."""
+
+    def __init__(self, world):
+        self.world = world
+        if world > 1:
+            import torch.distributed as td
+            td.init_process_group("gloo")
+            self.td = td
+
+    def barrier(self):
+        if self.world > 1:
+            self.td.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        self.td.all_reduce(t, op=self.td.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.td.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="gqa_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash(name):
+    with open(os.path.join(ROOT, "gqa_attention_kv_decode_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file, key):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
+    source is unchanged since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[key]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_sha256_16") != kernel_source_hash(kernel_file):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- decode workload
+
+def make_layers(S, dtype, device, n_layers=LAYERS, B=1, hq=HQ, hkv=HKV, d=D):
+    return [inputs.qkv(B, hq, hkv, d, 1, S, dtype, layer=l, device=device) for l in range(n_layers)]
+
+
+def time_decode_step(binding, layers, outs, ws, S, stream, evs=None):
+    """One step: the 28 layer calls.  With `evs`, each launch is bracketed
+    by events (start, end) appended to the list."""
+    scale = D ** -0.5
+    for (q, k, v), o in zip(layers, outs):
+        if evs is not None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        binding.gqa_attn_decode(q, k, v, o, None, scale, ws, max_kv_len=S, stream=stream)
+        if evs is not None:
+            e1.record(stream)
+            evs.append((e0, e1))
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def sweep_point(binding, S, dtype, device, stream, flush, iters=20, graph=True):
+    """µs per layer call for 28 calls at kv_len S (cold L2 per sequence)."""
+    layers = make_layers(S, dtype, device)
+    outs = [torch.empty_like(q) for q, _, _ in layers]
+    ws = binding.decode_workspace(1, HQ, HKV, D, S, binding._dtype_code(layers[0][0]), device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            time_decode_step(binding, layers, outs, ws, S, stream)
+    res = {}
+    modes = ["launch"]
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            time_decode_step(binding, layers, outs, ws, S, stream)
+        modes.append("graph")
+    for mode in modes:
+        ts = []
+        for _ in range(iters):
+            with torch.cuda.stream(stream):
+                flush_l2(flush)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if mode == "graph":
+                    g.replay()
+                else:
+                    time_decode_step(binding, layers, outs, ws, S, stream)
+                e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / LAYERS)
+        us = statistics.median(ts)
+        nbytes = metrics.decode_bytes(HQ, HKV, D, [S], layers[0][0].element_size())
+        res[mode] = {"us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+                     "p10_us": round(float(np.percentile(ts, 10)), 3),
+                     "p90_us": round(float(np.percentile(ts, 90)), 3)}
+    del layers, outs, ws, g
+    torch.cuda.empty_cache()
+    return res
+
+
+def ragged_point(binding, B, device, stream, flush, iters=10):
+    """Hq=32, Hkv=8, D=128, bf16, lengths uniform in [64, 8192], 36 layers."""
+    kv_lens = inputs.ragged_kv_lens(B, 64, 8192, seed=inputs.BASE_SEED + B)
+    lens_t = torch.from_numpy(kv_lens).to(device)
+    n_layers = 36
+    layers = make_layers(8192, torch.bfloat16, device, n_layers=n_layers, B=B, hq=32, hkv=8)
+    outs = [torch.empty_like(q) for q, _, _ in layers]
+    ws = binding.decode_workspace(B, 32, 8, 128, 8192, binding.GQA_BF16, device)
+
+    def step():
+        for (q, k, v), o in zip(layers, outs):
+            binding.gqa_attn_decode(q, k, v, o, lens_t, 128 ** -0.5, ws, max_kv_len=8192, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    ts = []
+    for _ in range(iters):
+        with torch.cuda.stream(stream):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n_layers)
+    us = statistics.median(ts)
+    nbytes = metrics.decode_bytes(32, 8, 128, kv_lens, 2)
+    del layers, outs
+    torch.cuda.empty_cache()
+    return {"B": B, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+ORACLE_SAMPLE = ("one KV head group (7 query heads, 1 of 4) of one layer call at kv_len=32768, "
+                 "fp32 inputs widened to fp64; GB/s scaled by that sample's algorithmic bytes")
+
+
+def _oracle_sample_worker(n_steps, seed_layer, conn):
+    # runs in a spawned process with single-threaded BLAS (cores = 1)
+    import numpy as _np
+    import oracle as _oracle
+    from gqa_attention_kv_decode_gb300 import inputs as _inputs
+    import torch as _torch
+    q, k, v = _inputs.qkv(1, HQ, HKV, D, 1, S_HEAD, _torch.float32, layer=seed_layer)
+    qs = q[:, 0:7].numpy()
+    ks = k[:, 0:1].numpy()
+    vs = v[:, 0:1].numpy()
+    times = []
+    for _ in range(n_steps):
+        t0 = time.perf_counter()
+        _oracle.attention(qs, ks, vs, scale=D ** -0.5)
+        times.append(time.perf_counter() - t0)
+    conn.send(times)
+    conn.close()
+
+
+def cpu_oracle_times(n_steps):
+    import multiprocessing as mp
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        parent, child = ctx.Pipe()
+        p = ctx.Process(target=_oracle_sample_worker, args=(n_steps, 0, child))
+        p.start()
+        times = parent.recv()
+        p.join()
+    finally:
+        for k, val in saved.items():
+            if val is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = val
+    return times
+
+
+def oracle_sample_bytes():
+    return 2 * 1 * S_HEAD * D * 4 + 2 * 7 * D * 4
+
+
+def cpu_baseline(n_steps=3):
+    times = cpu_oracle_times(n_steps)
+    t = statistics.median(times)
+    return {"value": round(oracle_sample_bytes() / t / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": ORACLE_SAMPLE + f"; median of {n_steps} runs",
+            "seconds_per_sample": round(t, 3)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    times = cpu_oracle_times(args.warmup + args.steps)[args.warmup:]
+    t = sum(times) / len(times)
+    value = oracle_sample_bytes() / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": ORACLE_SAMPLE},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": ORACLE_SAMPLE},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gqa", choices=["gqa", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import __graft_entry__
+    from gqa_attention_kv_decode_gb300 import binding
+
+    world, rank, local = dist_env()
+    dist = Dist(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    dist.barrier()
+    binding.lib()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+
+    # CPU baseline first (spawned process, before any large device allocation)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline()
+
+    stream = torch.cuda.Stream(device)
+    S = S_HEAD
+    layers = make_layers(S, torch.float32, device)
+    outs = [torch.empty_like(q) for q, _, _ in layers]
+    ws = binding.decode_workspace(1, HQ, HKV, D, S, binding.GQA_F32, device)
+    step_bytes = LAYERS * metrics.decode_bytes(HQ, HKV, D, [S], 4)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            time_decode_step(binding, layers, outs, ws, S, stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            time_decode_step(binding, layers, outs, ws, S, stream, evs)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = dist.max(t_start.elapsed_time(t_end))
+    ms_per_step = elapsed_ms / args.steps
+    launch_us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    avg_launch_us = sum(launch_us) / len(launch_us)
+    per_launch_bytes = metrics.decode_bytes(HQ, HKV, D, [S], 4)
+    achieved = per_launch_bytes / avg_launch_us / 1e3
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e_steps = 3
+    host = [(q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()) for q, k, v in layers]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(q.numel() * q.element_size() + k.numel() * k.element_size() + v.numel() * v.element_size()
+              for q, k, v in host)
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+
+    def e2e_step():
+        for (hq, hk, hv), (q, k, v) in zip(host, layers):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+        time_decode_step(binding, layers, outs, ws, S, stream)
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    del host, host_out
+
+    traffic = recorded_traffic("decode.cu", "decode_f32_d128_nrep7_S32768")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": S,
+                   "layers_per_step": LAYERS, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (3.76 GB per step on distinct buffers); no flush needed"},
+        "hbm_fraction": round(value / world / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "kernel": "decode_split_kernel<float,128,7,32,3>",
+                     "peak_source": peak_src, "avg_launch_us": round(avg_launch_us, 3)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": len(evs),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    del layers, outs, ws
+    torch.cuda.empty_cache()
+
+    if rank == 0 and world == 1 and not args.no_extras:
+        flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
+        sweep = {}
+        for dtype, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+            for s in (128, 256, 512, 1024, 2048, 4096, 32768):
+                sweep[f"{name}_S{s}"] = sweep_point(binding, s, dtype, device, stream, flush)
+        line["decode_sweep_qwen7b_28_layers"] = sweep
+        line["ragged_decode_qwen3_4b_36_layers"] = [ragged_point(binding, B, device, stream, flush)
+                                                   for B in (1, 2, 4, 8, 16, 64)]
+        del flush
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

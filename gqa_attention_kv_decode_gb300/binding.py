@@ -1,0 +1,250 @@
+"""ctypes binding over libgqa_attn.so (include/gqa_attn.h).
+
+The functions named like the C entry points take torch tensors, check that
+they are dense (the C ABI cannot see strides), pass ``data_ptr()`` values,
+sizes and the CUDA stream handle, and raise ``GqaAttnError`` on a non-zero
+status.  Every step of the computation runs in the library's kernels; there
+is no Python or CPU implementation behind these names.  If the library has
+not been built, the first call raises instead of falling back to anything.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgqa_attn.so")
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = -1
+GQA_ERR_UNSUPPORTED = -2
+GQA_ERR_NOT_DEVICE_PTR = -3
+GQA_ERR_CUDA = -4
+GQA_ERR_WORKSPACE = -5
+
+GQA_F32 = 0
+GQA_BF16 = 1
+
+GQA_DEV_KVLEN_CLAMPED = 1
+GQA_DEV_EMPTY_REQUEST = 2
+GQA_DEV_WAIT_TIMEOUT = 4
+
+EXPORTED = (
+    "gqa_attn_decode_workspace_size",
+    "gqa_attn_decode",
+    "gqa_attn_decode_q4_workspace_size",
+    "gqa_attn_decode_q4",
+    "gqa_attn_prefill",
+    "gqa_attn_status_string",
+    "gqa_attn_read_device_status",
+    "gqa_attn_clear_device_status",
+    "gqa_attn_decode_num_splits",
+    "gqa_attn_version",
+)
+
+_lib = None
+
+
+class GqaAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().gqa_attn_status_string(status).decode()
+        super().__init__(f"{where}: {msg} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libgqa_attn.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m gqa_attention_kv_decode_gb300.build` "
+            "(there is no CPU or Python fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    L.gqa_attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.gqa_attn_decode_workspace_size.restype = sz
+    L.gqa_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    L.gqa_attn_decode.restype = i32
+    L.gqa_attn_decode_q4_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.gqa_attn_decode_q4_workspace_size.restype = sz
+    L.gqa_attn_decode_q4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+    L.gqa_attn_decode_q4.restype = i32
+    L.gqa_attn_prefill.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+    L.gqa_attn_prefill.restype = i32
+    L.gqa_attn_status_string.argtypes = [i32]
+    L.gqa_attn_status_string.restype = ctypes.c_char_p
+    L.gqa_attn_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    L.gqa_attn_read_device_status.restype = i32
+    L.gqa_attn_clear_device_status.argtypes = [vp, vp]
+    L.gqa_attn_clear_device_status.restype = i32
+    L.gqa_attn_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.gqa_attn_decode_num_splits.restype = i32
+    L.gqa_attn_version.argtypes = []
+    L.gqa_attn_version.restype = i32
+    _lib = L
+    return L
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GQA_F32
+    if t.dtype == torch.bfloat16:
+        return GQA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libgqa_attn must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != GQA_OK:
+        raise GqaAttnError(rc, where)
+
+
+# --- entry points (same names as the C ABI) ----------------------------------
+
+def gqa_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
+    return lib().gqa_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, dtype)
+
+
+def gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
+    return lib().gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype)
+
+
+def gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len=None, stream=None):
+    """q, o [B,Hq,1,D]; k, v [B,Hkv,S_cap,D]; kv_lens int32 [B] or None."""
+    B, Hq, Tq, D = q.shape
+    Hkv, S_cap = k.shape[1], k.shape[2]
+    if Tq != 1:
+        raise ValueError("decode takes one query row per request")
+    if max_kv_len is None:
+        max_kv_len = S_cap
+    rc = lib().gqa_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(kv_lens), B, Hq, Hkv, D,
+                               S_cap, int(max_kv_len), float(scale), _dtype_code(q),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check(rc, "gqa_attn_decode")
+
+
+def gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len) -> int:
+    return lib().gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len)
+
+
+def gqa_attn_decode_q4(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, o, kv_lens, scale,
+                       workspace, max_kv_len=None, group_size=64, stream=None):
+    """q, o bf16 [B,Hq,1,D]; codes uint8 [B,Hkv,S_cap,D/2]; scale/bias fp16 [B,Hkv,S_cap,D/G]."""
+    B, Hq, Tq, D = q.shape
+    Hkv, S_cap = k_codes.shape[1], k_codes.shape[2]
+    if q.dtype != torch.bfloat16 or o.dtype != torch.bfloat16:
+        raise TypeError("q4 decode takes bf16 q and o")
+    if max_kv_len is None:
+        max_kv_len = S_cap
+    rc = lib().gqa_attn_decode_q4(_ptr(q), _ptr(k_codes), _ptr(k_scale), _ptr(k_bias),
+                                  _ptr(v_codes), _ptr(v_scale), _ptr(v_bias), _ptr(o),
+                                  _ptr(kv_lens), B, Hq, Hkv, D, S_cap, int(max_kv_len),
+                                  int(group_size), float(scale), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gqa_attn_decode_q4")
+
+
+def gqa_attn_prefill(q, k, v, o, kv_len, scale, causal=True, stream=None):
+    """q, o [B,Hq,q_len,D]; k, v [B,Hkv,S_cap,D]; keys 0..kv_len-1 visible."""
+    B, Hq, q_len, D = q.shape
+    Hkv, S_cap = k.shape[1], k.shape[2]
+    rc = lib().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, D, q_len,
+                                int(kv_len), S_cap, float(scale), 1 if causal else 0,
+                                _dtype_code(q), _stream(stream))
+    _check(rc, "gqa_attn_prefill")
+
+
+def gqa_attn_status_string(status: int) -> str:
+    return lib().gqa_attn_status_string(status).decode()
+
+
+def gqa_attn_read_device_status(workspace, stream=None) -> int:
+    out = ctypes.c_uint32(0)
+    _check(lib().gqa_attn_read_device_status(_ptr(workspace), ctypes.byref(out), _stream(stream)),
+           "gqa_attn_read_device_status")
+    return out.value
+
+
+def gqa_attn_clear_device_status(workspace, stream=None):
+    _check(lib().gqa_attn_clear_device_status(_ptr(workspace), _stream(stream)),
+           "gqa_attn_clear_device_status")
+
+
+def gqa_attn_version() -> int:
+    return lib().gqa_attn_version()
+
+
+# --- conveniences: allocate outputs / workspaces with torch, then call -------
+
+def decode_workspace(B, Hq, Hkv, D, max_kv_len, dtype, device="cuda") -> torch.Tensor:
+    n = gqa_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, dtype)
+    if n == 0:
+        raise ValueError("invalid decode shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_q4_workspace(B, Hq, Hkv, D, max_kv_len, device="cuda") -> torch.Tensor:
+    n = gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len)
+    if n == 0:
+        raise ValueError("invalid decode shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode(q, k, v, kv_lens=None, scale=None, max_kv_len=None, workspace=None, stream=None):
+    B, Hq, _, D = q.shape
+    Hkv, S_cap = k.shape[1], k.shape[2]
+    max_kv_len = S_cap if max_kv_len is None else int(max_kv_len)
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, D, max_kv_len, _dtype_code(q), q.device)
+    o = torch.empty_like(q)
+    gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len, stream)
+    return o
+
+
+def decode_q4(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, kv_lens=None, scale=None,
+              max_kv_len=None, workspace=None, stream=None):
+    B, Hq, _, D = q.shape
+    Hkv, S_cap = k_codes.shape[1], k_codes.shape[2]
+    max_kv_len = S_cap if max_kv_len is None else int(max_kv_len)
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = decode_q4_workspace(B, Hq, Hkv, D, max_kv_len, q.device)
+    o = torch.empty_like(q)
+    gqa_attn_decode_q4(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, o, kv_lens, scale,
+                       workspace, max_kv_len, stream=stream)
+    return o
+
+
+def prefill(q, k, v, kv_len=None, scale=None, causal=True, stream=None):
+    D = q.shape[-1]
+    kv_len = k.shape[2] if kv_len is None else int(kv_len)
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty_like(q)
+    gqa_attn_prefill(q, k, v, o, kv_len, scale, causal, stream)
+    return o

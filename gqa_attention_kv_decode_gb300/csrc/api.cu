@@ -1,0 +1,290 @@
+// api.cu -- the extern "C" boundary of libgqa_attn.so: argument validation,
+// the split-KV planner, workspace sizing and kernel dispatch.  Every check
+// runs on the host before anything is launched.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <mutex>
+
+#include "gqa_attn.h"
+#include "internal.h"
+
+namespace gqa {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static long ceil_div(long a, long b) { return (a + b - 1) / b; }
+
+// Chooses how many key splits each (request, KV head) gets so that the grid
+// covers about two CTAs per SM when requests are few and short, while a
+// split stays at least two tiles long and at most 1024 rows (so the splits
+// of long, ragged requests balance across the SMs).  GQA_ATTN_SPLITS, when
+// set, forces the split count (tuning only).
+SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms) {
+  SplitPlan p;
+  const int n_rep = Hq / Hkv;
+  p.tile = tile;
+  p.n_hc = (n_rep + 7) / 8;
+  p.nrep_cta = int(ceil_div(n_rep, p.n_hc));
+  const long units = long(B) * Hkv * p.n_hc;
+  const long target = 2L * (num_sms > 0 ? num_sms : 1);
+  long chunk = ceil_div(long(max_kv_len) * units, target);
+  chunk = ceil_div(chunk, tile) * tile;
+  const long lo = 2L * tile;
+  const long hi = (1024 / tile) * tile;
+  if (chunk < lo) chunk = lo;
+  if (chunk > hi) chunk = hi;
+  if (const char* env = std::getenv("GQA_ATTN_SPLITS")) {
+    const long n = std::atol(env);
+    if (n > 0) chunk = ceil_div(ceil_div(max_kv_len, n), tile) * tile;
+  }
+  if (ceil_div(max_kv_len, chunk) > 1024) chunk = ceil_div(ceil_div(max_kv_len, 1024), tile) * tile;
+  p.chunk = int(chunk);
+  p.n_split = int(ceil_div(max_kv_len, chunk));
+  return p;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+namespace {
+
+bool is_device_ptr(const void* p, int dev) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state of this query
+    return false;
+  }
+  if (attr.type == cudaMemoryTypeDevice) return attr.device == dev;
+  if (attr.type == cudaMemoryTypeManaged) return true;
+  return false;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common decode-shape checks; returns GQA_OK or an error code.
+int check_decode_shape(int B, int Hq, int Hkv, int D, int S_cap, int max_kv_len, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || S_cap < 1) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (max_kv_len < 1 || max_kv_len > S_cap) return GQA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_INVALID_ARG;
+  if (B > 65535) return GQA_ERR_INVALID_ARG;
+  const int n_hc = (Hq / Hkv + 7) / 8;
+  if (long(Hkv) * n_hc > 65535) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ptrs, int dev, size_t align) {
+  for (const void* p : ptrs) {
+    if (p == nullptr) return GQA_ERR_INVALID_ARG;
+    if (!aligned(p, align)) return GQA_ERR_INVALID_ARG;
+  }
+  for (const void* p : ptrs)
+    if (!is_device_ptr(p, dev)) return GQA_ERR_NOT_DEVICE_PTR;
+  return GQA_OK;
+}
+
+size_t decode_ws_size(int B, int Hq, int Hkv, int D, int max_kv_len, int tile) {
+  const SplitPlan p = plan_splits(B, Hq, Hkv, max_kv_len, tile, device_sm_count());
+  return workspace_layout(B, Hq, Hkv, p.n_hc, p.n_split, D).total;
+}
+
+}  // namespace
+
+extern "C" {
+
+GQA_ATTN_API int gqa_attn_version(void) { return 100; }
+
+GQA_ATTN_API const char* gqa_attn_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: invalid shape, length, scale or alignment";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: no kernel for this dtype / head size";
+    case GQA_ERR_NOT_DEVICE_PTR: return "GQA_ERR_NOT_DEVICE_PTR: a pointer is not device memory of the current device (there is no CPU path)";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE: workspace missing or smaller than *_workspace_size()";
+    default: return "unknown gqa_attn status";
+  }
+}
+
+GQA_ATTN_API size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_len,
+                                                   int dtype) {
+  if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return 0;
+  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_tile_rows(dtype, D));
+}
+
+GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
+                                            int dtype) {
+  if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count()).n_split;
+}
+
+GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, void* o,
+                                 const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int S_cap,
+                                 int max_kv_len, float scale, int dtype, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_kv_len, scale);
+  if (rc != GQA_OK) return rc;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  rc = check_ptrs({q, k, v, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  if (kv_lens != nullptr) {
+    rc = check_ptrs({kv_lens}, dev, 4);
+    if (rc != GQA_OK) return rc;
+  }
+  if (workspace == nullptr) return GQA_ERR_WORKSPACE;
+  rc = check_ptrs({workspace}, dev, 256);
+  if (rc == GQA_ERR_INVALID_ARG) return GQA_ERR_WORKSPACE;
+  if (rc != GQA_OK) return rc;
+
+  DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.kv_lens = kv_lens;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S_cap = S_cap;
+  a.max_kv_len = max_kv_len;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.workspace = workspace;
+  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count());
+  if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
+    return GQA_ERR_WORKSPACE;
+  if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+GQA_ATTN_API size_t gqa_attn_decode_q4_workspace_size(int B, int Hq, int Hkv, int D,
+                                                      int max_kv_len) {
+  if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
+  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_q4_tile_rows(D));
+}
+
+GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes, const uint16_t* k_scale,
+                                    const uint16_t* k_bias, const uint8_t* v_codes,
+                                    const uint16_t* v_scale, const uint16_t* v_bias, void* o,
+                                    const int32_t* kv_lens, int B, int Hq, int Hkv, int D,
+                                    int S_cap, int max_kv_len, int group_size, float scale,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_kv_len, scale);
+  if (rc != GQA_OK) return rc;
+  if (group_size != 64 || D % group_size != 0) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  rc = check_ptrs({q, k_codes, v_codes, k_scale, k_bias, v_scale, v_bias, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  if (kv_lens != nullptr) {
+    rc = check_ptrs({kv_lens}, dev, 4);
+    if (rc != GQA_OK) return rc;
+  }
+  if (workspace == nullptr) return GQA_ERR_WORKSPACE;
+  rc = check_ptrs({workspace}, dev, 256);
+  if (rc == GQA_ERR_INVALID_ARG) return GQA_ERR_WORKSPACE;
+  if (rc != GQA_OK) return rc;
+
+  DecodeQ4Args a;
+  a.q = q;
+  a.k_codes = k_codes;
+  a.k_scale = k_scale;
+  a.k_bias = k_bias;
+  a.v_codes = v_codes;
+  a.v_scale = v_scale;
+  a.v_bias = v_bias;
+  a.o = o;
+  a.kv_lens = kv_lens;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S_cap = S_cap;
+  a.max_kv_len = max_kv_len;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_q4_tile_rows(D), device_sm_count());
+  if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
+    return GQA_ERR_WORKSPACE;
+  const cudaError_t e = launch_decode_q4(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, void* o, int B,
+                                  int Hq, int Hkv, int D, int q_len, int kv_len, int S_cap,
+                                  float scale, int causal, int dtype, void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (q_len < 1 || kv_len < 1 || kv_len > S_cap || q_len > kv_len) return GQA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_BF16 || D != 64) return GQA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  const int rc = check_ptrs({q, k, v, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.q_len = q_len;
+  a.kv_len = kv_len;
+  a.S_cap = S_cap;
+  a.scale = scale;
+  a.causal = causal;
+  const cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+GQA_ATTN_API int gqa_attn_read_device_status(const void* workspace, uint32_t* out, void* stream) {
+  if (workspace == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  if (!is_device_ptr(workspace, dev)) return GQA_ERR_NOT_DEVICE_PTR;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(out, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+GQA_ATTN_API int gqa_attn_clear_device_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  if (!is_device_ptr(workspace, dev)) return GQA_ERR_NOT_DEVICE_PTR;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: fused grouped-query attention (GQA)
+ * over a KV cache, hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (all entry points): for request b, query head h and query
+ * row i,
+ *     O[b,h,i,:] = softmax_j( scale * Q[b,h,i,:] . K[b,g,j,:] ) V[b,g,j,:],
+ *     g = h / (Hq / Hkv),
+ * over the visible keys j < kv_len (and, when causal, j <= i + kv_len - q_len).
+ * The kernels read the Hkv unexpanded KV heads directly: no repeat_kv copy
+ * and no [Hq, q_len, kv_len] score matrix is ever written to memory.
+ *   - "2x Faster Qwen2 Decode on Metal in Candle", section "Why It Matters:
+ *     7x KV Expansion on Every Decode Step": the fused single-token kernel
+ *     indexes the KV heads through the query/KV head ratio in one pass.
+ *   - "Fused attention makes a 4,096-token Qwen2 prefill on Metal 4.5x
+ *     faster", section "Cause and workaround", items 1-3: K and V are given
+ *     before repeat_kv (Hq a multiple of Hkv); the causal mask aligns the
+ *     queries to the end of the keys; the rows of each head are contiguous.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) on the
+ *     current device; the library never copies from host memory and has no
+ *     CPU implementation.  A host pointer is rejected with
+ *     GQA_ERR_NOT_DEVICE_PTR before anything is launched.
+ *   - Layouts are dense, row-major:
+ *        Q, O : [B, Hq, q_len, D]      (q_len = 1 for decode)
+ *        K, V : [B, Hkv, S_cap, D]     rows of one head contiguous; head
+ *                                      stride S_cap*D, batch stride Hkv*S_cap*D
+ *     Only rows j < kv_len of K and V are read; rows past kv_len may hold
+ *     anything, including NaN.  Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream; the library never
+ *     synchronises the device.
+ *   - The library allocates no device memory.  Scratch memory (the split-KV
+ *     partials) is a caller-owned `workspace` whose size the matching
+ *     *_workspace_size() call returns for the current device.  The workspace
+ *     must be zero-filled once before its first use (e.g. cudaMemset); the
+ *     library leaves it ready for the next call afterwards.  Two calls that
+ *     may run concurrently on the GPU must not share a workspace.
+ *   - Arguments are validated on the host before any launch; on failure the
+ *     call returns a negative gqa_status_t and launches nothing.
+ *   - Per-request lengths that are out of range on the device are clamped
+ *     and reported through a status word at the start of the workspace
+ *     (GQA_DEV_* bits, OR-accumulated until cleared).
+ */
+#ifndef GQA_ATTN_H_
+#define GQA_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_ATTN_API __attribute__((visibility("default")))
+
+typedef enum gqa_status {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = -1,    /* bad shape, length, scale or pointer alignment */
+  GQA_ERR_UNSUPPORTED = -2,    /* valid, but no kernel for this dtype / D        */
+  GQA_ERR_NOT_DEVICE_PTR = -3, /* a pointer is not device memory                 */
+  GQA_ERR_CUDA = -4,           /* a CUDA runtime call or launch failed            */
+  GQA_ERR_WORKSPACE = -5       /* workspace missing or too small                  */
+} gqa_status_t;
+
+typedef enum gqa_dtype {
+  GQA_F32 = 0,  /* Q, K, V, O in float32; fp32 arithmetic                         */
+  GQA_BF16 = 1  /* Q, K, V, O in bfloat16; fp32 accumulation, output rounded RNE */
+} gqa_dtype_t;
+
+/* Device status bits (OR-accumulated in the first 4 bytes of a workspace). */
+#define GQA_DEV_KVLEN_CLAMPED 1u /* some kv_lens[b] < 0 or > max_kv_len: clamped */
+#define GQA_DEV_EMPTY_REQUEST 2u /* some kv_lens[b] == 0: that output is zeros    */
+#define GQA_DEV_WAIT_TIMEOUT 4u  /* a bounded wait on a tile copy gave up          */
+
+/* ---------------------------------------------------------------------------
+ * Single-token decode (q_len = 1), split-KV with a log-sum-exp combine.
+ *
+ * Defines: the fused decode attention of "2x Faster Qwen2 Decode on Metal in
+ * Candle" ("Why It Matters"; benchmark geometry of sections 2.1 and 2.2),
+ * batched across requests with per-request lengths ("Batching Decode
+ * Attention Across Requests ...", VeloxQuant-MLX blog, "Part 4": the B axis
+ * of the fused decode-attend grid).
+ *
+ *   q        [B, Hq, 1, D]       dtype
+ *   k, v     [B, Hkv, S_cap, D]  dtype
+ *   o        [B, Hq, 1, D]       dtype (written)
+ *   kv_lens  device int32 [B], number of valid rows per request; NULL means
+ *            every request has max_kv_len rows.  A value < 0 or > max_kv_len
+ *            is clamped into [0, max_kv_len] and sets GQA_DEV_KVLEN_CLAMPED;
+ *            0 writes a zero output row and sets GQA_DEV_EMPTY_REQUEST.
+ *   max_kv_len  host upper bound of kv_lens (1 <= max_kv_len <= S_cap); it
+ *            sizes the grid and the workspace.
+ *   scale    softmax scale, finite and > 0 (usually 1/sqrt(D)).
+ *   dtype    GQA_F32 or GQA_BF16.   D in {64, 128}.   Hq % Hkv == 0.
+ * Returns GQA_OK or a negative gqa_status_t.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int D,
+                                                   int max_kv_len, int dtype);
+
+GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, void* o,
+                                 const int32_t* kv_lens, int B, int Hq, int Hkv, int D,
+                                 int S_cap, int max_kv_len, float scale, int dtype,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-token decode over a 4-bit group-affine quantized KV cache, with the
+ * dequantisation done inside the attention loop (no fp16/bf16 copy of the
+ * cache is made).
+ *
+ * Defines: the fused group-affine decode-attend of "Batching Decode Attention
+ * Across Requests Got Us 3.83x ..." (VeloxQuant-MLX blog, "The setup" and
+ * "Part 4": codes, per-group scales and biases, GROUP_SIZE, a B axis).
+ * Element d of a cached row is x = code[d] * scale[d / G] + bias[d / G].
+ *
+ *   q        bf16 [B, Hq, 1, D];  o bf16 [B, Hq, 1, D] (written)
+ *   k_codes, v_codes  uint8 [B, Hkv, S_cap, D/2]: element 2t in the low
+ *            nibble of byte t, element 2t+1 in the high nibble
+ *   k_scale, k_bias, v_scale, v_bias  fp16 (raw uint16 bits)
+ *            [B, Hkv, S_cap, D/G]
+ *   group_size  G, must be 64;  D in {64, 128}
+ *   kv_lens, max_kv_len, scale, workspace, stream: as gqa_attn_decode.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API size_t gqa_attn_decode_q4_workspace_size(int B, int Hq, int Hkv, int D,
+                                                      int max_kv_len);
+
+GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes,
+                                    const uint16_t* k_scale, const uint16_t* k_bias,
+                                    const uint8_t* v_codes, const uint16_t* v_scale,
+                                    const uint16_t* v_bias, void* o, const int32_t* kv_lens,
+                                    int B, int Hq, int Hkv, int D, int S_cap, int max_kv_len,
+                                    int group_size, float scale, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Prefill (q_len >= 1 query rows per request), causal or not, on the
+ * tcgen05 tensor cores with accumulators in tensor memory.
+ *
+ * Defines: the fused causal prefill of "Fused attention makes a 4,096-token
+ * Qwen2 prefill on Metal 4.5x faster" ("Cause and workaround"): one pass
+ * over the grouped KV heads, causal mask inside the kernel, queries aligned
+ * to the END of the keys, so a chunk of q_len queries at offset
+ * kv_len - q_len sees every earlier key (chunked prefill).
+ *
+ *   q, o     bf16 [B, Hq, q_len, D];  k, v  bf16 [B, Hkv, S_cap, D]
+ *   kv_len   keys visible to the last query row (q_len <= kv_len <= S_cap),
+ *            the same for every request
+ *   causal   1: key j visible to query row i iff j <= i + kv_len - q_len;
+ *            0: every key j < kv_len visible
+ *   dtype    GQA_BF16 (fp32 accumulation).   D == 64.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, void* o,
+                                  int B, int Hq, int Hkv, int D, int q_len, int kv_len,
+                                  int S_cap, float scale, int causal, int dtype,
+                                  void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Helpers
+ * ------------------------------------------------------------------------- */
+/* Static, human-readable name of a gqa_status_t. */
+GQA_ATTN_API const char* gqa_attn_status_string(int status);
+
+/* Copies the device status word of `workspace` to *out after the work queued
+ * on `stream` so far has finished (synchronises that stream). */
+GQA_ATTN_API int gqa_attn_read_device_status(const void* workspace, uint32_t* out,
+                                             void* stream);
+
+/* Zeroes the device status word of `workspace` (asynchronous on `stream`). */
+GQA_ATTN_API int gqa_attn_clear_device_status(void* workspace, void* stream);
+
+/* Number of splits along the keys the decode entry points use for this
+ * problem on the current device (the grid's x extent); exposed for tests. */
+GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
+                                            int dtype);
+
+/* ABI version (major * 100 + minor). */
+GQA_ATTN_API int gqa_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H_ */
