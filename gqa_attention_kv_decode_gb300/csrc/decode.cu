@@ -23,10 +23,11 @@
 //     rescaled, when a tile's maximum exceeds it by more than 2^8;
 //   * P.V: a lane owns one 16-byte column chunk of V for every head, rows are
 //     spread over row slots, p is broadcast from shared memory;
-//   * the split's (max, sum, unnormalised o) go to the workspace; the last CTA
-//     of a (b, g, head chunk) to arrive merges all splits in split order
-//     (log-sum-exp combine), writes O and resets its arrival counter.  A
-//     request that fits one split writes O directly.
+//   * the split's (max, sum, unnormalised o) go to the workspace and are
+//     merged by a two-level log-sum-exp tree inside the same kernel: the last
+//     CTA of each group of 8 splits merges the group, the last group merges
+//     the groups and writes O.  A request that fits one split writes O
+//     directly.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -50,6 +51,9 @@ struct DecodeParams {
   int32_t* counters;
   float2* ml;
   float* part_o;
+  float2* ml1;  // level-1 merged partials [B][Hq][n_groups_max]
+  float* o1;    // [B][Hq][n_groups_max][D]
+  int n_groups_max;
   uint64_t wait_limit_ns;
 };
 
@@ -90,7 +94,7 @@ struct Cfg {
   static_assert(R >= 1 && R * RG == TILE && R <= 8, "tile must give 1..8 rows per thread");
   static_assert(NV <= NREP_P, "head layout");
   static_assert(SLOTS * NREP_P * D * 4 <= NSTAGE * STAGEB, "reduction scratch must fit");
-  static_assert(1024 * 8 * 4 <= NSTAGE * STAGEB, "combine weights must fit");
+  static_assert((128 * 8 + 16) * 4 <= NSTAGE * STAGEB, "merge weights must fit");
   static_assert(NREP >= 1 && NREP <= 8, "at most 8 query heads per CTA");
 };
 
@@ -174,9 +178,10 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const DecodeParams p)
   const int cp = tid % C::LPR;
   const int slot = tid / C::LPR;
 
-  float m_ref[C::NREP_P];
-#pragma unroll
-  for (int h = 0; h < C::NREP_P; ++h) m_ref[h] = -INFINITY;
+  // Running reference (log2 units) of head hl; other heads' values are
+  // fetched from lane h by shuffle (keeps them out of local memory).
+  const int hl = lane % C::NREP_P;
+  float my_mref = -INFINITY;
   float l_part[C::NV];
 #pragma unroll
   for (int i = 0; i < C::NV; ++i) l_part[i] = 0.f;
@@ -288,39 +293,35 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const DecodeParams p)
       __syncthreads();
       return;
     }
-    float alpha[C::NREP_P];
-    bool any = false;
+    float my_alpha = 1.f;
+    {
+      float tm = wmax[hl];
 #pragma unroll
-    for (int h = 0; h < C::NREP_P; ++h) {
-      float tm = wmax[h];
-#pragma unroll
-      for (int w = 1; w < C::NWARP; ++w) tm = fmaxf(tm, wmax[w * 8 + h]);
-      if (tm > m_ref[h] + 8.f) {
-        alpha[h] = fast_exp2(m_ref[h] - tm);
-        m_ref[h] = tm;
-        any = true;
-      } else {
-        alpha[h] = 1.f;
+      for (int w = 1; w < C::NWARP; ++w) tm = fmaxf(tm, wmax[w * 8 + hl]);
+      if (tm > my_mref + 8.f) {
+        my_alpha = fast_exp2(my_mref - tm);
+        my_mref = tm;
       }
     }
+    const bool any = __any_sync(0xffffffffu, my_alpha != 1.f);
 #pragma unroll
     for (int i = 0; i < C::NV; ++i) {
-      float mr = m_ref[0], al = alpha[0];
-#pragma unroll
-      for (int h = 1; h < C::NREP_P; ++h)
-        if (hd[i] == h) { mr = m_ref[h]; al = alpha[h]; }
+      const float mr = __shfl_sync(0xffffffffu, my_mref, hd[i]);
+      const float al = __shfl_sync(0xffffffffu, my_alpha, hd[i]);
       const float pv = s[i] == -INFINITY ? 0.f : fast_exp2(s[i] - mr);
       l_part[i] = l_part[i] * al + pv;
       if (ds * C::NV + i < C::R * C::NREP_P) p_s[rowi[i] * C::NREP_P + hd[i]] = make_float2(pv, pv);
     }
     if (any) {
 #pragma unroll
-      for (int h = 0; h < NREP; ++h)
+      for (int h = 0; h < NREP; ++h) {
+        const float a = __shfl_sync(0xffffffffu, my_alpha, h);
 #pragma unroll
         for (int j = 0; j < C::EPC / 2; ++j) {
-          acc_o[h][j].x *= alpha[h];
-          acc_o[h][j].y *= alpha[h];
+          acc_o[h][j].x *= a;
+          acc_o[h][j].y *= a;
         }
+      }
     }
     __syncthreads();
 
@@ -373,6 +374,7 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const DecodeParams p)
 #pragma unroll
       for (int i = 0; i < C::NV; ++i) wsum[warp * 8 + lane * C::NV + i] = ls[i];
   }
+  if (warp == 0 && lane < C::NREP_P) wmax[lane] = my_mref;  // final references
   float* red = reinterpret_cast<float*>(smem);  // all tile copies have been consumed
 #pragma unroll
   for (int h = 0; h < NREP; ++h)
@@ -395,53 +397,102 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const DecodeParams p)
     } else {
       p.part_o[((ws_row + h) * p.n_split + split) * D + d] = sum;
       if (d == 0) {
-        float mr = m_ref[0];
-#pragma unroll
-        for (int hh = 1; hh < C::NREP_P; ++hh)
-          if (hh == h) mr = m_ref[hh];
-        p.ml[(ws_row + h) * p.n_split + split] = make_float2(mr, lt);
+        p.ml[(ws_row + h) * p.n_split + split] = make_float2(wmax[h], lt);
       }
     }
   }
   if (n_used == 1) return;
 
-  // ---- arrival count; the last split of this (b, g, head chunk) combines ----
+  // ---- combine: a two-level tree over groups of GS splits ----
+  // The last CTA of a group to arrive merges the group's partials (at most
+  // GS of them); with one group that merge is final.  Otherwise it writes a
+  // level-1 partial, and the last group to finish merges the level-1
+  // partials.  Merges run in split order, so the result does not depend on
+  // which CTA arrives last.  Counters are reset by the CTA that consumes them.
+  constexpr int GS = 8;
+  const int n_groups = (n_used + GS - 1) / GS;
+  const int grp = split / GS;
+  const int gsize = min(GS, n_used - grp * GS);
+  int32_t* cnt = p.counters + ((size_t(b) * p.Hkv + g) * p.n_hc + hc) * (p.n_groups_max + 1);
+  float* wts = reinterpret_cast<float*>(smem);  // [<=128 sources][8 heads] merge weights
+  float* stat = wts + 128 * 8;                  // merged max [8], merged sum [8]
+
+  // Merges sources [first, first+count) of the per-head lists (ml, o) whose
+  // head stride is `hs` slots.  final: normalise and write O; otherwise write
+  // the unnormalised level-1 partial into slot `grp`.
+  auto merge = [&](const float2* mlb, const float* ob, int hs, int first, int count, bool final_) {
+    for (int h = warp; h < nh; h += C::NWARP) {
+      const float2* mlh = mlb + (ws_row + h) * hs + first;
+      float M = -INFINITY;
+      for (int sidx = lane; sidx < count; sidx += 32) M = fmaxf(M, __ldcg(&mlh[sidx]).x);
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+      float Ls = 0.f;
+      for (int sidx = lane; sidx < count; sidx += 32) {
+        const float2 x = __ldcg(&mlh[sidx]);
+        const float w = fast_exp2(x.x - M);
+        wts[sidx * 8 + h] = w;
+        Ls += x.y * w;
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
+      if (final_) {
+        const float inv = 1.f / Ls;
+        for (int sidx = lane; sidx < count; sidx += 32) wts[sidx * 8 + h] *= inv;
+      } else if (lane == 0) {
+        stat[h] = M;
+        stat[8 + h] = Ls;
+      }
+    }
+    __syncthreads();
+    constexpr int D4 = D / 4;
+    for (int pos = tid; pos < nh * D4; pos += C::NTHR) {
+      const int h = pos / D4, c4 = pos % D4;
+      const float4* src = reinterpret_cast<const float4*>(ob + ((ws_row + h) * hs + first) * D) + c4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int sidx = 0; sidx < count; ++sidx) {
+        const float4 x = __ldcg(src + size_t(sidx) * D4);
+        const float w = wts[sidx * 8 + h];
+        acc.x += x.x * w;
+        acc.y += x.y * w;
+        acc.z += x.z * w;
+        acc.w += x.w * w;
+      }
+      if (final_) {
+        T* dst = out + (ws_row + h) * D + c4 * 4;
+        store_f(dst + 0, acc.x);
+        store_f(dst + 1, acc.y);
+        store_f(dst + 2, acc.z);
+        store_f(dst + 3, acc.w);
+      } else {
+        reinterpret_cast<float4*>(p.o1 + ((ws_row + h) * p.n_groups_max + grp) * D)[c4] = acc;
+      }
+    }
+    if (!final_ && tid < nh)
+      p.ml1[(ws_row + tid) * p.n_groups_max + grp] = make_float2(stat[tid], stat[8 + tid]);
+  };
+
   __threadfence();
   __syncthreads();
-  int32_t* counter = p.counters + (size_t(b) * p.Hkv + g) * p.n_hc + hc;
-  if (tid == 0) flag[1] = (atomicAdd(counter, 1) == n_used - 1);
+  if (tid == 0) flag[1] = (atomicAdd(&cnt[grp], 1) == gsize - 1);
   __syncthreads();
   if (!flag[1]) return;
   __threadfence();
-
-  float* wts = reinterpret_cast<float*>(smem);  // [n_used][8] combine weights
-  for (int h = warp; h < nh; h += C::NWARP) {
-    const float2* mlh = p.ml + (ws_row + h) * p.n_split;
-    float M = -INFINITY;
-    for (int sidx = lane; sidx < n_used; sidx += 32) M = fmaxf(M, __ldcg(&mlh[sidx]).x);
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-    float Ls = 0.f;
-    for (int sidx = lane; sidx < n_used; sidx += 32) {
-      const float2 x = __ldcg(&mlh[sidx]);
-      const float w = fast_exp2(x.x - M);
-      wts[sidx * 8 + h] = w;
-      Ls += x.y * w;
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
-    const float inv = 1.f / Ls;
-    for (int sidx = lane; sidx < n_used; sidx += 32) wts[sidx * 8 + h] *= inv;
+  if (tid == 0) cnt[grp] = 0;
+  if (n_groups == 1) {
+    merge(p.ml, p.part_o, p.n_split, 0, n_used, true);
+    return;
   }
+  merge(p.ml, p.part_o, p.n_split, grp * GS, gsize, false);
+  __threadfence();
   __syncthreads();
-  for (int e = tid; e < nh * D; e += C::NTHR) {
-    const int h = e / D, d = e % D;
-    const float* po = p.part_o + (ws_row + h) * size_t(p.n_split) * D + d;
-    float acc = 0.f;
-    for (int sidx = 0; sidx < n_used; ++sidx) acc += __ldcg(po + size_t(sidx) * D) * wts[sidx * 8 + h];
-    store_f(out + (ws_row + h) * D + d, acc);
-  }
-  if (tid == 0) *counter = 0;
+  if (tid == 0) flag[1] = (atomicAdd(&cnt[p.n_groups_max], 1) == n_groups - 1);
+  __syncthreads();
+  if (!flag[1]) return;
+  __threadfence();
+  if (tid == 0) cnt[p.n_groups_max] = 0;
+  merge(p.ml1, p.o1, p.n_groups_max, 0, n_groups, true);
 }
 
 template <typename T, int D, int NREP, int TILE, int NSTAGE>
@@ -509,11 +560,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.n_split = a.plan.n_split;
   p.qscale = float(double(a.scale) * 1.4426950408889634);
   const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, a.plan.n_split, a.D);
+  p.n_groups_max = w.n_groups_max;
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
+  p.ml1 = reinterpret_cast<float2*>(ws + w.off_ml1);
+  p.o1 = reinterpret_cast<float*>(ws + w.off_o1);
   p.wait_limit_ns = kWaitLimitNs;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   if (a.dtype == GQA_F32)
