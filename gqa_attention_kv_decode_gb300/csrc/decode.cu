@@ -8,7 +8,8 @@
 // copies them).
 //
 // Data flow per CTA:
-//   * the split's key rows [s0, s1) are streamed in tiles of TILE rows; each
+//   * the split's key rows are streamed in tiles of TILE rows, tiles dealt
+//     round-robin to the splits; each
 //     tile of K and of V is one contiguous bulk (TMA) copy into shared memory
 //     (rows of a head are contiguous: "Fused attention makes a 4,096-token
 //     Qwen2 prefill ...", "Cause and workaround", item 3), NSTAGE tiles in
@@ -23,11 +24,10 @@
 //     rescaled, when a tile's maximum exceeds it by more than 2^8;
 //   * P.V: a lane owns one 16-byte column chunk of V for every head, rows are
 //     spread over row slots, p is broadcast from shared memory;
-//   * the split's (max, sum, unnormalised o) go to the workspace and are
-//     merged by a two-level log-sum-exp tree inside the same kernel: the last
-//     CTA of each group of 8 splits merges the group, the last group merges
-//     the groups and writes O.  A request that fits one split writes O
-//     directly.
+//   * a request that fits one split writes O directly; otherwise each split
+//     writes (max, sum, unnormalised o) to the workspace and a second, small
+//     kernel (one CTA per request and query head, launched with programmatic
+//     dependent launch) merges them with the log-sum-exp rule, in split order.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -48,12 +48,8 @@ struct DecodeParams {
   int B, Hq, Hkv, n_rep, n_hc, nrep_cta, S_cap, max_kv_len, chunk, n_split;
   float qscale;  // scale * log2(e)
   uint32_t* status;
-  int32_t* counters;
-  float2* ml;
-  float* part_o;
-  float2* ml1;  // level-1 merged partials [B][Hq][n_groups_max]
-  float* o1;    // [B][Hq][n_groups_max][D]
-  int n_groups_max;
+  float2* ml;     // [B][Hq][n_split] (max in log2 units, sum)
+  float* part_o;  // [B][Hq][n_split][D] unnormalised partial outputs
   uint64_t wait_limit_ns;
 };
 
@@ -62,45 +58,67 @@ __device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloa
 __device__ __forceinline__ void store_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <typename T, int D, int NREP, int TILE, int NSTAGE>
+template <typename T, int D, int NREP, int R_, int NSTAGE>
 struct Cfg {
   static constexpr int E = sizeof(T);
   static constexpr int ROWB = D * E;     // bytes per key row
   static constexpr int NCH = ROWB / 16;  // 16-byte chunks per row
   static constexpr int EPC = 16 / E;     // elements per chunk
   static constexpr int NPART = EPC / 4;  // float4 pieces of q per chunk
-  static constexpr int NTHR = 128;
-  static constexpr int NWARP = NTHR / 32;
+  static constexpr int NCW = 4;          // consumer warps
+  static constexpr int NWARP = NCW + 1;  // + one producer warp
+  static constexpr int NTHR = 32 * NWARP;
   static constexpr int DS = 8;           // lanes sharing a row in the score phase
   static constexpr int NIT = NCH / DS;
-  static constexpr int RG = NTHR / DS;   // row groups
-  static constexpr int R = TILE / RG;    // rows per thread in the score phase
+  static constexpr int R = R_;           // rows per lane in the score phase
+  static constexpr int TW = 4 * R;       // rows per consumer warp per tile
+  static constexpr int TILE = NCW * TW;
   static constexpr int NREP_P = NREP <= 1 ? 1 : NREP <= 2 ? 2 : NREP <= 4 ? 4 : 8;
   static constexpr int VP = (R * NREP_P > 8) ? R * NREP_P : 8;
   static constexpr int NV = VP / 8;      // complete scores per lane after the butterfly
   static constexpr int G = NREP_P / NV;  // distinct head sets among the 8 lanes of a row group
   static constexpr int LPR = NCH;        // lanes per row in the P.V phase
-  static constexpr int SLOTS = NTHR / LPR;
+  static constexpr int RPW = 32 / LPR;   // rows a warp covers per P.V step
   static constexpr int TILEB = TILE * ROWB;
   static constexpr int STAGEB = 2 * TILEB;
   static constexpr int OFF_Q = NSTAGE * STAGEB;
   static constexpr int OFF_P = OFF_Q + NREP_P * D * 4;
-  static constexpr int OFF_WMAX = OFF_P + TILE * NREP_P * 8;
-  static constexpr int OFF_WSUM = OFF_WMAX + NWARP * 8 * 4;
-  static constexpr int OFF_BAR = OFF_WSUM + NWARP * 8 * 4;
-  static constexpr int OFF_FLAG = OFF_BAR + NSTAGE * 8;
+  static constexpr int OFF_BAR = OFF_P + NCW * TW * NREP_P * 8;
+  static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
   static constexpr int SMEM = OFF_FLAG + 16;
+  static constexpr int MERGE_FLOATS = NCW * (NREP_P * D + 2 * NREP_P);
   static_assert(NCH % DS == 0, "row must split into 8 lanes of 16-byte chunks");
-  static_assert(R >= 1 && R * RG == TILE && R <= 8, "tile must give 1..8 rows per thread");
-  static_assert(NV <= NREP_P, "head layout");
-  static_assert(SLOTS * NREP_P * D * 4 <= NSTAGE * STAGEB, "reduction scratch must fit");
-  static_assert((128 * 8 + 16) * 4 <= NSTAGE * STAGEB, "merge weights must fit");
+  static_assert(LPR <= 32 && 32 % LPR == 0, "a warp covers whole rows in P.V");
+  static_assert(TW % RPW == 0, "P.V steps tile the warp's rows");
+  static_assert(NV <= NREP_P && R <= 8, "head layout");
+  static_assert(MERGE_FLOATS * 4 <= NSTAGE * STAGEB, "warp-merge scratch must fit");
+  static_assert((128 * 8 + 16) * 4 <= NSTAGE * STAGEB, "split-merge weights must fit");
   static_assert(NREP >= 1 && NREP <= 8, "at most 8 query heads per CTA");
 };
 
-template <typename T, int D, int NREP, int TILE, int NSTAGE>
-__global__ void __launch_bounds__(128) decode_split_kernel(const DecodeParams p) {
-  using C = Cfg<T, D, NREP, TILE, NSTAGE>;
+// Waits for `parity` of `bar`.  Gives up (returns false) when another warp
+// has raised the abort flag, or after `limit_ns`, in which case it raises it.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <typename T, int D, int NREP, int R_, int NSTAGE>
+__global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
+    decode_split_kernel(const DecodeParams p) {
+  using C = Cfg<T, D, NREP, R_, NSTAGE>;
+  constexpr int TILE = C::TILE;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -128,377 +146,431 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const DecodeParams p)
   }
   const int n_used = (L + p.chunk - 1) / p.chunk;
   if (split >= n_used) return;
-  const int s0 = split * p.chunk;
-  const int s1 = min(s0 + p.chunk, L);
-  const int nt = (s1 - s0 + TILE - 1) / TILE;
+  // Tiles are dealt round-robin to the request's n_used splits: split s
+  // takes tiles s, s + n_used, ...  At any moment the CTAs of one head then
+  // stream one dense region of the cache instead of n_used far-apart ones.
+  const int nt_all = (L + TILE - 1) / TILE;
+  const int nt = (nt_all - split + n_used - 1) / n_used;
 
   float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
   float2* p_s = reinterpret_cast<float2*>(smem + C::OFF_P);
-  float* wmax = reinterpret_cast<float*>(smem + C::OFF_WMAX);
-  float* wsum = reinterpret_cast<float*>(smem + C::OFF_WSUM);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + NSTAGE;
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [1] last [2] issued
 
   const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
   const unsigned char* kbase = static_cast<const unsigned char*>(p.k) + head_row0 * C::ROWB;
   const unsigned char* vbase = static_cast<const unsigned char*>(p.v) + head_row0 * C::ROWB;
 
-  auto issue = [&](int t, int st, uint64_t pol) {
-    const int row0 = s0 + t * TILE;
-    const uint32_t bytes = uint32_t(min(TILE, s1 - row0)) * C::ROWB;
+  // Copy k-th tile of this split into stage st (one elected thread).
+  auto issue = [&](int kt, int st, uint64_t pol) {
+    const int row0 = (split + kt * n_used) * TILE;
+    const uint32_t bytes = uint32_t(min(TILE, L - row0)) * C::ROWB;
     unsigned char* dst = smem + st * C::STAGEB;
-    mbar_arrive_expect_tx(&bar[st], 2 * bytes);
-    bulk_g2s(dst, kbase + size_t(row0) * C::ROWB, bytes, &bar[st], pol);
-    bulk_g2s(dst + C::TILEB, vbase + size_t(row0) * C::ROWB, bytes, &bar[st], pol);
+    mbar_arrive_expect_tx(&full[st], 2 * bytes);
+    bulk_g2s(dst, kbase + size_t(row0) * C::ROWB, bytes, &full[st], pol);
+    bulk_g2s(dst + C::TILEB, vbase + size_t(row0) * C::ROWB, bytes, &full[st], pol);
   };
-
-  uint64_t pol = 0;
-  if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
+  if (tid == 0) {  // barriers, then the first NSTAGE copies before q is staged
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NCW);
+    }
     fence_barrier_init();
     flag[0] = 0;
-    pol = l2_policy_evict_first();
+    flag[1] = 0;
+    const uint64_t pol = l2_policy_evict_first();
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t, pol);
+    flag[2] = min(NSTAGE, nt);
   }
-  // q rows of this CTA's heads, pre-scaled, laid out so that the 8 lanes of a
-  // row group read 8 consecutive 16-byte pieces: [h][part][chunk][4]
+  // q rows of this CTA's heads (contiguous in memory), pre-scaled, laid out so
+  // that the 8 lanes of a row group read 8 consecutive 16-byte pieces:
+  // [h][part][chunk][4].  Every thread issues its (at most two) 16-byte loads
+  // before storing anything, so staging costs one memory round trip.
   {
-    const T* qg = static_cast<const T*>(p.q);
-    for (int e = tid; e < C::NREP_P * D; e += C::NTHR) {
-      const int h = e / D, d = e % D;
-      const float val = h < nh ? load_f(qg + (size_t(b) * p.Hq + h0 + h) * D + d) * p.qscale : 0.f;
-      const int c = d / C::EPC, part = (d % C::EPC) / 4, j = d % 4;
-      q_s[((h * C::NPART + part) * C::NCH + c) * 4 + j] = val;
+    constexpr int NVEC_MAX = (C::NREP_P * D * C::E / 16 + C::NTHR - 1) / C::NTHR;
+    const int nvec = nh * D * C::E / 16;
+    const uint4* qg = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                     (size_t(b) * p.Hq + h0) * D);
+    uint4 raw[NVEC_MAX];
+#pragma unroll
+    for (int k = 0; k < NVEC_MAX; ++k) {
+      const int vi = tid + k * C::NTHR;
+      if (vi < nvec) raw[k] = qg[vi];
     }
+#pragma unroll
+    for (int k = 0; k < NVEC_MAX; ++k) {
+      const int vi = tid + k * C::NTHR;
+      if (vi < nvec) {
+        const int h = vi / C::NCH, c = vi % C::NCH;  // one 16-byte vector = one chunk
+        float* dst = q_s + (h * C::NPART * C::NCH + c) * 4;
+        if constexpr (sizeof(T) == 4) {
+          *reinterpret_cast<float4*>(dst) =
+              make_float4(__uint_as_float(raw[k].x) * p.qscale, __uint_as_float(raw[k].y) * p.qscale,
+                          __uint_as_float(raw[k].z) * p.qscale, __uint_as_float(raw[k].w) * p.qscale);
+        } else {
+          const float2 a0 = bf16x2_to_float2(raw[k].x), a1 = bf16x2_to_float2(raw[k].y);
+          const float2 a2 = bf16x2_to_float2(raw[k].z), a3 = bf16x2_to_float2(raw[k].w);
+          *reinterpret_cast<float4*>(dst) =
+              make_float4(a0.x * p.qscale, a0.y * p.qscale, a1.x * p.qscale, a1.y * p.qscale);
+          *reinterpret_cast<float4*>(dst + C::NCH * 4) =
+              make_float4(a2.x * p.qscale, a2.y * p.qscale, a3.x * p.qscale, a3.y * p.qscale);
+        }
+      }
+    }
+    for (int e = nh * D + tid; e < C::NREP_P * D; e += C::NTHR) q_s[e] = 0.f;  // padded heads
   }
   __syncthreads();
 
-  const int ds = tid & 7;
-  const int rg = tid >> 3;
-  const int cp = tid % C::LPR;
-  const int slot = tid / C::LPR;
-
-  // Running reference (log2 units) of head hl; other heads' values are
-  // fetched from lane h by shuffle (keeps them out of local memory).
-  const int hl = lane % C::NREP_P;
-  float my_mref = -INFINITY;
-  float l_part[C::NV];
-#pragma unroll
-  for (int i = 0; i < C::NV; ++i) l_part[i] = 0.f;
-  float2 acc_o[NREP][C::EPC / 2];
-#pragma unroll
-  for (int h = 0; h < NREP; ++h)
-#pragma unroll
-    for (int j = 0; j < C::EPC / 2; ++j) acc_o[h][j] = make_float2(0.f, 0.f);
-
-  for (int t = 0; t < nt; ++t) {
-    const int st = t % NSTAGE;
-    const uint32_t par = uint32_t(t / NSTAGE) & 1u;
-    if (!mbar_wait_bounded(&bar[st], par, p.wait_limit_ns)) flag[0] = 1;
-    const int nvalid = min(TILE, s1 - (s0 + t * TILE));
-    const unsigned char* Ks = smem + st * C::STAGEB;
-    const unsigned char* Vs = Ks + C::TILEB;
-
-    // ---- scores: R rows x NREP heads per thread, D split over 8 lanes ----
-    float2 acc[C::R][NREP];
-#pragma unroll
-    for (int r = 0; r < C::R; ++r)
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) acc[r][h] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int it = 0; it < C::NIT; ++it) {
-      const int c = it * C::DS + ds;
-      float2 kf[C::R][C::EPC / 2];
-#pragma unroll
-      for (int r = 0; r < C::R; ++r) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(Ks + (rg * C::R + r) * C::ROWB + c * 16);
-        if constexpr (sizeof(T) == 4) {
-          kf[r][0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
-          kf[r][1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
-        } else {
-          kf[r][0] = bf16x2_to_float2(raw.x);
-          kf[r][1] = bf16x2_to_float2(raw.y);
-          kf[r][2] = bf16x2_to_float2(raw.z);
-          kf[r][3] = bf16x2_to_float2(raw.w);
-        }
+  float* merge_s = reinterpret_cast<float*>(smem);  // aliases the stages after the loop
+  if (warp == C::NCW) {
+    // ---------------- producer warp: one lane streams the tiles ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      for (int t = NSTAGE; t < nt; ++t) {
+        const int st = t % NSTAGE;
+        if (!wait_or_abort(&empty[st], uint32_t(t / NSTAGE - 1) & 1u, flag, p.wait_limit_ns)) break;
+        issue(t, st, pol);
+        flag[2] = t + 1;
       }
+    }
+  } else {
+    // ---------------- consumer warps: rows [warp*TW, warp*TW + TW) of each tile ----------------
+    const int ds = lane & 7;
+    const int rg = lane >> 3;
+    const int cp = lane % C::LPR;
+    const int rsub = lane / C::LPR;
+    float2* pw = p_s + warp * C::TW * C::NREP_P;
+    float mref[C::NV], lsum[C::NV];
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) {
+    for (int i = 0; i < C::NV; ++i) {
+      mref[i] = -INFINITY;
+      lsum[i] = 0.f;
+    }
+    float2 acc_o[NREP][C::EPC / 2];
 #pragma unroll
-        for (int part = 0; part < C::NPART; ++part) {
-          const float4 qv =
-              *reinterpret_cast<const float4*>(q_s + ((h * C::NPART + part) * C::NCH + c) * 4);
-          const float2 qa = make_float2(qv.x, qv.y), qb = make_float2(qv.z, qv.w);
+    for (int h = 0; h < NREP; ++h)
+#pragma unroll
+      for (int j = 0; j < C::EPC / 2; ++j) acc_o[h][j] = make_float2(0.f, 0.f);
+
+    for (int t = 0; t < nt; ++t) {
+      const int st = t % NSTAGE;
+      const bool ok = wait_or_abort(&full[st], uint32_t(t / NSTAGE) & 1u, flag, p.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int nvalid = min(TILE, L - (split + t * n_used) * TILE);
+      const int wrow0 = warp * C::TW;
+      const int wvalid = min(C::TW, nvalid - wrow0);
+      const unsigned char* Ks = smem + st * C::STAGEB + wrow0 * C::ROWB;
+      const unsigned char* Vs = smem + st * C::STAGEB + C::TILEB + wrow0 * C::ROWB;
+      if (wvalid > 0) {
+        // ---- scores: R rows x NREP heads per lane, D split over 8 lanes ----
+        float2 acc[C::R][NREP];
+#pragma unroll
+        for (int r = 0; r < C::R; ++r)
+#pragma unroll
+          for (int h = 0; h < NREP; ++h) acc[r][h] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int it = 0; it < C::NIT; ++it) {
+          const int c = it * C::DS + ds;
+          float2 kf[C::R][C::EPC / 2];
 #pragma unroll
           for (int r = 0; r < C::R; ++r) {
-            acc[r][h] = ffma2(kf[r][2 * part], qa, acc[r][h]);
-            acc[r][h] = ffma2(kf[r][2 * part + 1], qb, acc[r][h]);
+            const uint4 raw = *reinterpret_cast<const uint4*>(Ks + (rg * C::R + r) * C::ROWB + c * 16);
+            if constexpr (sizeof(T) == 4) {
+              kf[r][0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+              kf[r][1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+            } else {
+              kf[r][0] = bf16x2_to_float2(raw.x);
+              kf[r][1] = bf16x2_to_float2(raw.y);
+              kf[r][2] = bf16x2_to_float2(raw.z);
+              kf[r][3] = bf16x2_to_float2(raw.w);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < NREP; ++h) {
+#pragma unroll
+            for (int part = 0; part < C::NPART; ++part) {
+              const float4 qv =
+                  *reinterpret_cast<const float4*>(q_s + ((h * C::NPART + part) * C::NCH + c) * 4);
+              const float2 qa = make_float2(qv.x, qv.y), qb = make_float2(qv.z, qv.w);
+#pragma unroll
+              for (int r = 0; r < C::R; ++r) {
+                acc[r][h] = ffma2(kf[r][2 * part], qa, acc[r][h]);
+                acc[r][h] = ffma2(kf[r][2 * part + 1], qb, acc[r][h]);
+              }
+            }
+          }
+        }
+        // transposing butterfly over the 8 lanes of a row group: afterwards
+        // lane ds holds the complete scores with flat index ds*NV + i, where
+        // the flat index of (row r, head h) is r*NREP_P + h.
+        float v[C::VP];
+#pragma unroll
+        for (int r = 0; r < C::R; ++r)
+#pragma unroll
+          for (int h = 0; h < C::NREP_P; ++h)
+            v[r * C::NREP_P + h] = h < NREP ? acc[r][h].x + acc[r][h].y : 0.f;
+#pragma unroll
+        for (int i = C::R * C::NREP_P; i < C::VP; ++i) v[i] = 0.f;
+#pragma unroll
+        for (int m = 4, n = C::VP; m >= 1; m >>= 1, n >>= 1) {
+          const bool hi = (ds & m) != 0;
+#pragma unroll
+          for (int i = 0; i < n / 2; ++i) {
+            const float mine = hi ? v[n / 2 + i] : v[i];
+            const float send = hi ? v[i] : v[n / 2 + i];
+            v[i] = mine + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+        // ---- online softmax over this warp's rows (base 2, lazy reference) ----
+        float sc[C::NV], mx[C::NV], alpha[C::NV];
+#pragma unroll
+        for (int i = 0; i < C::NV; ++i) {
+          const int idx = ds * C::NV + i;
+          const int r = idx / C::NREP_P, h = idx % C::NREP_P;
+          const bool valid = (idx < C::R * C::NREP_P) && (h < nh) && (rg * C::R + r < wvalid);
+          sc[i] = valid ? v[i] : -INFINITY;
+          mx[i] = sc[i];
+        }
+#pragma unroll
+        for (int m = C::G; m <= 16; m <<= 1)
+#pragma unroll
+          for (int i = 0; i < C::NV; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], m));
+        bool rescale = false;
+#pragma unroll
+        for (int i = 0; i < C::NV; ++i) {
+          alpha[i] = 1.f;
+          if (mx[i] > mref[i] + 8.f) {
+            alpha[i] = fast_exp2(mref[i] - mx[i]);
+            mref[i] = mx[i];
+            rescale = true;
+          }
+          const float pv = sc[i] == -INFINITY ? 0.f : fast_exp2(sc[i] - mref[i]);
+          lsum[i] = lsum[i] * alpha[i] + pv;
+          const int idx = ds * C::NV + i;
+          if (idx < C::R * C::NREP_P)
+            pw[(rg * C::R + idx / C::NREP_P) * C::NREP_P + idx % C::NREP_P] = make_float2(pv, pv);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int h = 0; h < NREP; ++h) {
+            const float a = __shfl_sync(0xffffffffu, alpha[h % C::NV], h / C::NV);
+#pragma unroll
+            for (int j = 0; j < C::EPC / 2; ++j) {
+              acc_o[h][j].x *= a;
+              acc_o[h][j].y *= a;
+            }
+          }
+        }
+        __syncwarp();
+        // ---- P.V: lane owns one 16-byte column chunk for every head ----
+        for (int j = rsub; j < wvalid; j += C::RPW) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(Vs + j * C::ROWB + cp * 16);
+          float2 vf[C::EPC / 2];
+          if constexpr (sizeof(T) == 4) {
+            vf[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+            vf[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+          } else {
+            vf[0] = bf16x2_to_float2(raw.x);
+            vf[1] = bf16x2_to_float2(raw.y);
+            vf[2] = bf16x2_to_float2(raw.z);
+            vf[3] = bf16x2_to_float2(raw.w);
+          }
+          const float2* prow = pw + j * C::NREP_P;
+          if constexpr (C::NREP_P == 1) {
+            const float2 pp = prow[0];
+#pragma unroll
+            for (int jj = 0; jj < C::EPC / 2; ++jj) acc_o[0][jj] = ffma2(vf[jj], pp, acc_o[0][jj]);
+          } else {
+#pragma unroll
+            for (int h2 = 0; h2 < C::NREP_P / 2; ++h2) {
+              if (2 * h2 >= NREP) break;
+              const float4 pp = reinterpret_cast<const float4*>(prow)[h2];
+#pragma unroll
+              for (int jj = 0; jj < C::EPC / 2; ++jj) {
+                acc_o[2 * h2][jj] = ffma2(vf[jj], make_float2(pp.x, pp.y), acc_o[2 * h2][jj]);
+                if (2 * h2 + 1 < NREP)
+                  acc_o[2 * h2 + 1][jj] = ffma2(vf[jj], make_float2(pp.z, pp.w), acc_o[2 * h2 + 1][jj]);
+              }
+            }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
-    // transposing butterfly over the 8 lanes of the row group: afterwards
-    // lane ds holds the complete scores with flat index ds*NV + i, where the
-    // flat index of (row r, head h) is r*NREP_P + h.
-    float v[C::VP];
-#pragma unroll
-    for (int r = 0; r < C::R; ++r)
-#pragma unroll
-      for (int h = 0; h < C::NREP_P; ++h)
-        v[r * C::NREP_P + h] = h < NREP ? acc[r][h].x + acc[r][h].y : 0.f;
-#pragma unroll
-    for (int i = C::R * C::NREP_P; i < C::VP; ++i) v[i] = 0.f;
-#pragma unroll
-    for (int m = 4, n = C::VP; m >= 1; m >>= 1, n >>= 1) {
-      const bool hi = (ds & m) != 0;
-#pragma unroll
-      for (int i = 0; i < n / 2; ++i) {
-        const float mine = hi ? v[n / 2 + i] : v[i];
-        const float send = hi ? v[i] : v[n / 2 + i];
-        v[i] = mine + __shfl_xor_sync(0xffffffffu, send, m);
-      }
-    }
-    float s[C::NV];
-    int hd[C::NV];
-    int rowi[C::NV];
-#pragma unroll
-    for (int i = 0; i < C::NV; ++i) {
-      const int idx = ds * C::NV + i;
-      const int r = idx / C::NREP_P;
-      hd[i] = idx % C::NREP_P;
-      rowi[i] = rg * C::R + r;
-      const bool valid = (idx < C::R * C::NREP_P) && (hd[i] < nh) && (rowi[i] < nvalid);
-      s[i] = valid ? v[i] : -INFINITY;
-    }
-    // per-head tile maximum: lanes whose ds agree modulo G hold the same heads
-    {
-      float mx[C::NV];
-#pragma unroll
-      for (int i = 0; i < C::NV; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int m = C::G; m <= 16; m <<= 1)
-#pragma unroll
-        for (int i = 0; i < C::NV; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], m));
-      if (lane < C::G)
-#pragma unroll
-        for (int i = 0; i < C::NV; ++i) wmax[warp * 8 + lane * C::NV + i] = mx[i];
-    }
-    __syncthreads();
-    if (flag[0]) {  // a tile copy did not arrive in time: record it and stop
-      if (tid == 0) {
-        atomicOr(p.status, GQA_DEV_WAIT_TIMEOUT);
-        for (int u = t; u < nt && u < t + NSTAGE; ++u)  // let issued copies land
-          mbar_wait_bounded(&bar[u % NSTAGE], uint32_t(u / NSTAGE) & 1u, p.wait_limit_ns);
-      }
-      __syncthreads();
-      return;
-    }
-    float my_alpha = 1.f;
-    {
-      float tm = wmax[hl];
-#pragma unroll
-      for (int w = 1; w < C::NWARP; ++w) tm = fmaxf(tm, wmax[w * 8 + hl]);
-      if (tm > my_mref + 8.f) {
-        my_alpha = fast_exp2(my_mref - tm);
-        my_mref = tm;
-      }
-    }
-    const bool any = __any_sync(0xffffffffu, my_alpha != 1.f);
-#pragma unroll
-    for (int i = 0; i < C::NV; ++i) {
-      const float mr = __shfl_sync(0xffffffffu, my_mref, hd[i]);
-      const float al = __shfl_sync(0xffffffffu, my_alpha, hd[i]);
-      const float pv = s[i] == -INFINITY ? 0.f : fast_exp2(s[i] - mr);
-      l_part[i] = l_part[i] * al + pv;
-      if (ds * C::NV + i < C::R * C::NREP_P) p_s[rowi[i] * C::NREP_P + hd[i]] = make_float2(pv, pv);
-    }
-    if (any) {
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) {
-        const float a = __shfl_sync(0xffffffffu, my_alpha, h);
-#pragma unroll
-        for (int j = 0; j < C::EPC / 2; ++j) {
-          acc_o[h][j].x *= a;
-          acc_o[h][j].y *= a;
-        }
-      }
-    }
-    __syncthreads();
 
-    // ---- P.V: lane owns one 16-byte column chunk for every head ----
-    for (int row = slot; row < nvalid; row += C::SLOTS) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(Vs + row * C::ROWB + cp * 16);
-      float2 vf[C::EPC / 2];
-      if constexpr (sizeof(T) == 4) {
-        vf[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
-        vf[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
-      } else {
-        vf[0] = bf16x2_to_float2(raw.x);
-        vf[1] = bf16x2_to_float2(raw.y);
-        vf[2] = bf16x2_to_float2(raw.z);
-        vf[3] = bf16x2_to_float2(raw.w);
-      }
-      const float2* prow = p_s + row * C::NREP_P;
-      if constexpr (C::NREP_P == 1) {
-        const float2 pp = prow[0];
-#pragma unroll
-        for (int j = 0; j < C::EPC / 2; ++j) acc_o[0][j] = ffma2(vf[j], pp, acc_o[0][j]);
-      } else {
-#pragma unroll
-        for (int h2 = 0; h2 < C::NREP_P / 2; ++h2) {
-          if (2 * h2 >= NREP) break;
-          const float4 pp = reinterpret_cast<const float4*>(prow)[h2];
-#pragma unroll
-          for (int j = 0; j < C::EPC / 2; ++j) {
-            acc_o[2 * h2][j] = ffma2(vf[j], make_float2(pp.x, pp.y), acc_o[2 * h2][j]);
-            if (2 * h2 + 1 < NREP)
-              acc_o[2 * h2 + 1][j] = ffma2(vf[j], make_float2(pp.z, pp.w), acc_o[2 * h2 + 1][j]);
-          }
-        }
-      }
-    }
-    __syncthreads();
-    if (tid == 0 && t + NSTAGE < nt) issue(t + NSTAGE, st, pol);
-  }
-
-  // ---- per-CTA reduction: softmax sums and row slots of o ----
-  {
-    float ls[C::NV];
-#pragma unroll
-    for (int i = 0; i < C::NV; ++i) ls[i] = l_part[i];
+    // ---- this warp's (max, sum, o) into the merge scratch ----
 #pragma unroll
     for (int m = C::G; m <= 16; m <<= 1)
 #pragma unroll
-      for (int i = 0; i < C::NV; ++i) ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], m);
-    if (lane < C::G)
+      for (int i = 0; i < C::NV; ++i) lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], m);
 #pragma unroll
-      for (int i = 0; i < C::NV; ++i) wsum[warp * 8 + lane * C::NV + i] = ls[i];
+    for (int m = 16; m >= C::LPR; m >>= 1)
+#pragma unroll
+      for (int h = 0; h < NREP; ++h)
+#pragma unroll
+        for (int j = 0; j < C::EPC / 2; ++j) {
+          acc_o[h][j].x += __shfl_xor_sync(0xffffffffu, acc_o[h][j].x, m);
+          acc_o[h][j].y += __shfl_xor_sync(0xffffffffu, acc_o[h][j].y, m);
+        }
+    // (A) consumers only: every consumer has left the tile loop, so all
+    // issued copies have landed and the stages can hold the merge scratch
+    // (after an abort copies may still be in flight: write nothing).
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+    float* mw = merge_s + C::NCW * C::NREP_P * D;
+    float* lw = mw + C::NCW * C::NREP_P;
+    if (!flag[0] && rsub == 0)
+#pragma unroll
+      for (int h = 0; h < NREP; ++h)
+#pragma unroll
+        for (int j = 0; j < C::EPC / 2; ++j)
+          *reinterpret_cast<float2*>(merge_s + (warp * C::NREP_P + h) * D + cp * C::EPC + 2 * j) =
+              acc_o[h][j];
+    if (!flag[0] && lane < C::G)
+#pragma unroll
+      for (int i = 0; i < C::NV; ++i) {
+        mw[warp * C::NREP_P + lane * C::NV + i] = mref[i];
+        lw[warp * C::NREP_P + lane * C::NV + i] = lsum[i];
+      }
   }
-  if (warp == 0 && lane < C::NREP_P) wmax[lane] = my_mref;  // final references
-  float* red = reinterpret_cast<float*>(smem);  // all tile copies have been consumed
-#pragma unroll
-  for (int h = 0; h < NREP; ++h)
-#pragma unroll
-    for (int j = 0; j < C::EPC / 2; ++j)
-      *reinterpret_cast<float2*>(red + (slot * C::NREP_P + h) * D + cp * C::EPC + 2 * j) = acc_o[h][j];
   __syncthreads();
+  // let the merge kernel's CTAs be scheduled while this grid drains
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
-  for (int e = tid; e < nh * D; e += C::NTHR) {
-    const int h = e / D, d = e % D;
-    float sum = 0.f;
-#pragma unroll
-    for (int sl = 0; sl < C::SLOTS; ++sl) sum += red[(sl * C::NREP_P + h) * D + d];
-    float lt = 0.f;
-#pragma unroll
-    for (int w = 0; w < C::NWARP; ++w) lt += wsum[w * 8 + h];
-    if (n_used == 1) {
-      store_f(out + (ws_row + h) * D + d, sum / lt);
-    } else {
-      p.part_o[((ws_row + h) * p.n_split + split) * D + d] = sum;
-      if (d == 0) {
-        p.ml[(ws_row + h) * p.n_split + split] = make_float2(wmax[h], lt);
-      }
-    }
-  }
-  if (n_used == 1) return;
-
-  // ---- combine: a two-level tree over groups of GS splits ----
-  // The last CTA of a group to arrive merges the group's partials (at most
-  // GS of them); with one group that merge is final.  Otherwise it writes a
-  // level-1 partial, and the last group to finish merges the level-1
-  // partials.  Merges run in split order, so the result does not depend on
-  // which CTA arrives last.  Counters are reset by the CTA that consumes them.
-  constexpr int GS = 8;
-  const int n_groups = (n_used + GS - 1) / GS;
-  const int grp = split / GS;
-  const int gsize = min(GS, n_used - grp * GS);
-  int32_t* cnt = p.counters + ((size_t(b) * p.Hkv + g) * p.n_hc + hc) * (p.n_groups_max + 1);
-  float* wts = reinterpret_cast<float*>(smem);  // [<=128 sources][8 heads] merge weights
-  float* stat = wts + 128 * 8;                  // merged max [8], merged sum [8]
-
-  // Merges sources [first, first+count) of the per-head lists (ml, o) whose
-  // head stride is `hs` slots.  final: normalise and write O; otherwise write
-  // the unnormalised level-1 partial into slot `grp`.
-  auto merge = [&](const float2* mlb, const float* ob, int hs, int first, int count, bool final_) {
-    for (int h = warp; h < nh; h += C::NWARP) {
-      const float2* mlh = mlb + (ws_row + h) * hs + first;
-      float M = -INFINITY;
-      for (int sidx = lane; sidx < count; sidx += 32) M = fmaxf(M, __ldcg(&mlh[sidx]).x);
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-      float Ls = 0.f;
-      for (int sidx = lane; sidx < count; sidx += 32) {
-        const float2 x = __ldcg(&mlh[sidx]);
-        const float w = fast_exp2(x.x - M);
-        wts[sidx * 8 + h] = w;
-        Ls += x.y * w;
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
-      if (final_) {
-        const float inv = 1.f / Ls;
-        for (int sidx = lane; sidx < count; sidx += 32) wts[sidx * 8 + h] *= inv;
-      } else if (lane == 0) {
-        stat[h] = M;
-        stat[8 + h] = Ls;
+  if (flag[0]) {  // a tile copy or a stage release did not arrive in time
+    if (tid == 0) {
+      atomicOr(p.status, GQA_DEV_WAIT_TIMEOUT);
+      const int issued = flag[2];
+      for (int s = 0; s < NSTAGE && s < issued; ++s) {  // let the last copy on each stage land
+        const int u = s + ((issued - 1 - s) / NSTAGE) * NSTAGE;
+        mbar_wait_bounded(&full[s], uint32_t(u / NSTAGE) & 1u, p.wait_limit_ns);
       }
     }
     __syncthreads();
-    constexpr int D4 = D / 4;
-    for (int pos = tid; pos < nh * D4; pos += C::NTHR) {
-      const int h = pos / D4, c4 = pos % D4;
-      const float4* src = reinterpret_cast<const float4*>(ob + ((ws_row + h) * hs + first) * D) + c4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int sidx = 0; sidx < count; ++sidx) {
-        const float4 x = __ldcg(src + size_t(sidx) * D4);
-        const float w = wts[sidx * 8 + h];
-        acc.x += x.x * w;
-        acc.y += x.y * w;
-        acc.z += x.z * w;
-        acc.w += x.w * w;
-      }
-      if (final_) {
-        T* dst = out + (ws_row + h) * D + c4 * 4;
-        store_f(dst + 0, acc.x);
-        store_f(dst + 1, acc.y);
-        store_f(dst + 2, acc.z);
-        store_f(dst + 3, acc.w);
-      } else {
-        reinterpret_cast<float4*>(p.o1 + ((ws_row + h) * p.n_groups_max + grp) * D)[c4] = acc;
-      }
-    }
-    if (!final_ && tid < nh)
-      p.ml1[(ws_row + tid) * p.n_groups_max + grp] = make_float2(stat[tid], stat[8 + tid]);
-  };
-
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) flag[1] = (atomicAdd(&cnt[grp], 1) == gsize - 1);
-  __syncthreads();
-  if (!flag[1]) return;
-  __threadfence();
-  if (tid == 0) cnt[grp] = 0;
-  if (n_groups == 1) {
-    merge(p.ml, p.part_o, p.n_split, 0, n_used, true);
     return;
   }
-  merge(p.ml, p.part_o, p.n_split, grp * GS, gsize, false);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) flag[1] = (atomicAdd(&cnt[p.n_groups_max], 1) == n_groups - 1);
-  __syncthreads();
-  if (!flag[1]) return;
-  __threadfence();
-  if (tid == 0) cnt[p.n_groups_max] = 0;
-  merge(p.ml1, p.o1, p.n_groups_max, 0, n_groups, true);
+
+  // ---- merge the consumer warps, then write O or this split's partial ----
+  const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
+  {
+    const float* mw = merge_s + C::NCW * C::NREP_P * D;
+    const float* lw = mw + C::NCW * C::NREP_P;
+    for (int e = tid; e < nh * D; e += C::NTHR) {
+      const int h = e / D, d = e % D;
+      float M = mw[h];
+#pragma unroll
+      for (int w = 1; w < C::NCW; ++w) M = fmaxf(M, mw[w * C::NREP_P + h]);
+      float lt = 0.f, sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NCW; ++w) {
+        const float mwv = mw[w * C::NREP_P + h];
+        const float ew = mwv == -INFINITY ? 0.f : fast_exp2(mwv - M);
+        lt += lw[w * C::NREP_P + h] * ew;
+        sum += merge_s[(w * C::NREP_P + h) * D + d] * ew;
+      }
+      if (n_used == 1) {
+        store_f(out + (ws_row + h) * D + d, sum / lt);
+      } else {
+        p.part_o[((ws_row + h) * p.n_split + split) * D + d] = sum;
+        if (d == 0) p.ml[(ws_row + h) * p.n_split + split] = make_float2(M, lt);
+      }
+    }
+  }
 }
 
-template <typename T, int D, int NREP, int TILE, int NSTAGE>
+// Merges the split partials of one (request, query head) row, after the split
+// kernel has finished (programmatic dependent launch: the grid may start
+// early; griddepcontrol.wait returns once the split kernel's writes are
+// visible).  All partial loads of a thread are issued before the weights are
+// known, so the merge costs about one L2 round trip.
+//   w_s = 2^(m_s - M) / sum_s l_s 2^(m_s - M),   o = sum_s w_s o_s,   M = max_s m_s
+template <typename T, int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  constexpr int D4 = D / 4;
+  constexpr int NSG = 256 / D4;  // split groups: thread (sg, c4) sums splits sg, sg + NSG, ...
+  constexpr int PRE = 8;         // partials held in registers per thread
+  __shared__ float w_s[1024];
+  __shared__ float4 red[NSG][D4];
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c4 = tid % D4, sg = tid / D4;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
+  L = L < 0 ? 0 : (L > p.max_kv_len ? p.max_kv_len : L);
+  const int n_used = (L + p.chunk - 1) / p.chunk;
+  if (n_used <= 1) return;  // written by the split kernel itself
+  const float2* ml = p.ml + size_t(bh) * p.n_split;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + size_t(bh) * p.n_split * D) + c4;
+  float4 x[PRE];
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int sidx = sg + k * NSG;
+    x[k] = sidx < n_used ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (warp == 0) {
+    float M = -INFINITY;
+    for (int sidx = lane; sidx < n_used; sidx += 32) M = fmaxf(M, __ldcg(&ml[sidx]).x);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+    float Ls = 0.f;
+    for (int sidx = lane; sidx < n_used; sidx += 32) {
+      const float2 v = __ldcg(&ml[sidx]);
+      const float w = fast_exp2(v.x - M);
+      w_s[sidx] = w;
+      Ls += v.y * w;
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
+    const float inv = 1.f / Ls;
+    for (int sidx = lane; sidx < n_used; sidx += 32) w_s[sidx] *= inv;
+  }
+  __syncthreads();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int sidx = sg + k * NSG;
+    if (sidx < n_used) {
+      const float w = w_s[sidx];
+      acc.x += x[k].x * w;
+      acc.y += x[k].y * w;
+      acc.z += x[k].z * w;
+      acc.w += x[k].w * w;
+    }
+  }
+  for (int sidx = sg + PRE * NSG; sidx < n_used; sidx += NSG) {
+    const float4 v = __ldcg(po + size_t(sidx) * D4);
+    const float w = w_s[sidx];
+    acc.x += v.x * w;
+    acc.y += v.y * w;
+    acc.z += v.z * w;
+    acc.w += v.w * w;
+  }
+  red[sg][c4] = acc;
+  __syncthreads();
+  if (tid < D4) {
+    float4 t = red[0][tid];
+#pragma unroll
+    for (int k = 1; k < NSG; ++k) {
+      const float4 v = red[k][tid];
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    T* dst = static_cast<T*>(p.o) + size_t(bh) * D + tid * 4;
+    store_f(dst + 0, t.x);
+    store_f(dst + 1, t.y);
+    store_f(dst + 2, t.z);
+    store_f(dst + 3, t.w);
+  }
+}
+
+template <typename T, int D, int NREP, int R, int NSTAGE>
 cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  using C = Cfg<T, D, NREP, TILE, NSTAGE>;
-  auto kern = decode_split_kernel<T, D, NREP, TILE, NSTAGE>;
+  using C = Cfg<T, D, NREP, R, NSTAGE>;
+  auto kern = decode_split_kernel<T, D, NREP, R, NSTAGE>;
   static bool configured = false;  // per instantiation; attribute is per-function
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -509,19 +581,38 @@ cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The merge grid (one CTA per request and query head) is launched with
+// programmatic stream serialisation, so its launch overlaps the split
+// kernel's tail; the kernel itself waits for the split kernel's results.
+template <typename T, int D>
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.B * p.Hq);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, p);
+}
+
 // Per (dtype, D): tile height and pipeline depth.  A stage (K + V tile) is
 // 32 KiB for the 128-dim heads; three stages keep ~64 KiB in flight per CTA
 // and two CTAs fit on an SM.
 template <typename T, int D>
 struct TileCfg;
-template <> struct TileCfg<float, 128> { static constexpr int TILE = 32, NSTAGE = 3; };
-template <> struct TileCfg<__nv_bfloat16, 128> { static constexpr int TILE = 64, NSTAGE = 3; };
-template <> struct TileCfg<float, 64> { static constexpr int TILE = 64, NSTAGE = 3; };
-template <> struct TileCfg<__nv_bfloat16, 64> { static constexpr int TILE = 64, NSTAGE = 4; };
+template <> struct TileCfg<float, 128> { static constexpr int R = 2, NSTAGE = 3, TILE = 32; };
+template <> struct TileCfg<__nv_bfloat16, 128> { static constexpr int R = 4, NSTAGE = 3, TILE = 64; };
+template <> struct TileCfg<float, 64> { static constexpr int R = 4, NSTAGE = 3, TILE = 64; };
+template <> struct TileCfg<__nv_bfloat16, 64> { static constexpr int R = 4, NSTAGE = 4, TILE = 64; };
 
 template <typename T, int D>
 cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
-  constexpr int TL = TileCfg<T, D>::TILE, NS = TileCfg<T, D>::NSTAGE;
+  constexpr int TL = TileCfg<T, D>::R, NS = TileCfg<T, D>::NSTAGE;
+  static_assert(Cfg<T, D, 8, TL, NS>::TILE == TileCfg<T, D>::TILE, "tile height");
   switch (p.nrep_cta) {
     case 1: return launch_one<T, D, 1, TL, NS>(p, grid, s);
     case 2: return launch_one<T, D, 2, TL, NS>(p, grid, s);
@@ -560,21 +651,23 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.n_split = a.plan.n_split;
   p.qscale = float(double(a.scale) * 1.4426950408889634);
   const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, a.plan.n_split, a.D);
-  p.n_groups_max = w.n_groups_max;
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
   p.status = reinterpret_cast<uint32_t*>(ws);
-  p.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
-  p.ml1 = reinterpret_cast<float2*>(ws + w.off_ml1);
-  p.o1 = reinterpret_cast<float*>(ws + w.off_o1);
   p.wait_limit_ns = kWaitLimitNs;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
+  cudaError_t e;
   if (a.dtype == GQA_F32)
-    return a.D == 128 ? dispatch_nrep<float, 128>(p, grid, stream)
-                      : dispatch_nrep<float, 64>(p, grid, stream);
-  return a.D == 128 ? dispatch_nrep<__nv_bfloat16, 128>(p, grid, stream)
-                    : dispatch_nrep<__nv_bfloat16, 64>(p, grid, stream);
+    e = a.D == 128 ? dispatch_nrep<float, 128>(p, grid, stream) : dispatch_nrep<float, 64>(p, grid, stream);
+  else
+    e = a.D == 128 ? dispatch_nrep<__nv_bfloat16, 128>(p, grid, stream)
+                   : dispatch_nrep<__nv_bfloat16, 64>(p, grid, stream);
+  if (e != cudaSuccess || a.plan.n_split == 1) return e;
+  if (a.dtype == GQA_F32)
+    return a.D == 128 ? launch_merge<float, 128>(p, stream) : launch_merge<float, 64>(p, stream);
+  return a.D == 128 ? launch_merge<__nv_bfloat16, 128>(p, stream)
+                    : launch_merge<__nv_bfloat16, 64>(p, stream);
 }
 
 }  // namespace gqa

@@ -9,28 +9,23 @@ namespace gqa {
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)   uint32 device status word (GQA_DEV_* bits) + padding
-//   counters   int32 [B][Hkv][n_hc][n_groups_max + 1] arrival counters of the
-//              merge tree (self-resetting: each is zeroed by its consumer)
 //   ml         float2 [B][Hq][n_split]      per-split (max in log2 units, sum)
 //   part_o     float  [B][Hq][n_split][D]   per-split unnormalised outputs
-//   ml1, o1    the same per group of 8 splits [B][Hq][n_groups_max](...)
+// Nothing in it has to start at zero except the status word.
 struct WorkspaceLayout {
-  int n_groups_max;
-  size_t off_counters, off_ml, off_o, off_ml1, off_o1, total;
+  size_t off_ml, off_o, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int n_hc, int n_split, int D) {
+  (void)Hkv;
+  (void)n_hc;
   WorkspaceLayout w;
-  w.n_groups_max = (n_split + 7) / 8;
   const size_t bh = size_t(B) * Hq;
-  w.off_counters = 256;
-  w.off_ml = align256(w.off_counters + sizeof(int32_t) * size_t(B) * Hkv * n_hc * (w.n_groups_max + 1));
+  w.off_ml = 256;
   w.off_o = align256(w.off_ml + sizeof(float) * 2 * bh * n_split);
-  w.off_ml1 = align256(w.off_o + sizeof(float) * bh * n_split * D);
-  w.off_o1 = align256(w.off_ml1 + sizeof(float) * 2 * bh * w.n_groups_max);
-  w.total = align256(w.off_o1 + sizeof(float) * bh * w.n_groups_max * D);
+  w.total = align256(w.off_o + sizeof(float) * bh * n_split * D);
   return w;
 }
 
