@@ -65,8 +65,8 @@ struct Cfg {
   static constexpr int NCH = ROWB / 16;  // 16-byte chunks per row
   static constexpr int EPC = 16 / E;     // elements per chunk
   static constexpr int NPART = EPC / 4;  // float4 pieces of q per chunk
-  static constexpr int NCW = 4;          // consumer warps
-  static constexpr int NWARP = NCW + 1;  // + one producer warp
+  static constexpr int NCW = 4;          // warps; each owns a quarter of every tile's rows
+  static constexpr int NWARP = NCW;
   static constexpr int NTHR = 32 * NWARP;
   static constexpr int DS = 8;           // lanes sharing a row in the score phase
   static constexpr int NIT = NCH / DS;
@@ -84,7 +84,7 @@ struct Cfg {
   static constexpr int OFF_Q = NSTAGE * STAGEB;
   static constexpr int OFF_P = OFF_Q + NREP_P * D * 4;
   static constexpr int OFF_BAR = OFF_P + NCW * TW * NREP_P * 8;
-  static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
+  static constexpr int OFF_FLAG = OFF_BAR + NSTAGE * 8 + NSTAGE * 4;
   static constexpr int SMEM = OFF_FLAG + 16;
   static constexpr int MERGE_FLOATS = NCW * (NREP_P * D + 2 * NREP_P);
   static_assert(NCH % DS == 0, "row must split into 8 lanes of 16-byte chunks");
@@ -115,7 +115,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 template <typename T, int D, int NREP, int R_, int NSTAGE>
-__global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
+__global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
     decode_split_kernel(const DecodeParams p) {
   using C = Cfg<T, D, NREP, R_, NSTAGE>;
   constexpr int TILE = C::TILE;
@@ -154,9 +154,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
 
   float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
   float2* p_s = reinterpret_cast<float2*>(smem + C::OFF_P);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + NSTAGE;
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [1] last [2] issued
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // copy landed
+  int* rel = reinterpret_cast<int*>(smem + C::OFF_BAR + NSTAGE * 8);  // warps done with a stage
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [2] issued
 
   const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
   const unsigned char* kbase = static_cast<const unsigned char*>(p.k) + head_row0 * C::ROWB;
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
   if (tid == 0) {  // barriers, then the first NSTAGE copies before q is staged
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NCW);
+      rel[s] = 0;
     }
     fence_barrier_init();
     flag[0] = 0;
@@ -223,19 +223,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
   __syncthreads();
 
   float* merge_s = reinterpret_cast<float*>(smem);  // aliases the stages after the loop
-  if (warp == C::NCW) {
-    // ---------------- producer warp: one lane streams the tiles ----------------
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      for (int t = NSTAGE; t < nt; ++t) {
-        const int st = t % NSTAGE;
-        if (!wait_or_abort(&empty[st], uint32_t(t / NSTAGE - 1) & 1u, flag, p.wait_limit_ns)) break;
-        issue(t, st, pol);
-        flag[2] = t + 1;
-      }
-    }
-  } else {
-    // ---------------- consumer warps: rows [warp*TW, warp*TW + TW) of each tile ----------------
+  // ---- every warp: rows [warp*TW, warp*TW + TW) of each tile.  The last
+  // warp to finish with a stage refills it (no dedicated producer). ----
+  const uint64_t pol = l2_policy_evict_first();
     const int ds = lane & 7;
     const int rg = lane >> 3;
     const int cp = lane % C::LPR;
@@ -397,7 +387,16 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
+      if (lane == 0) {
+        __threadfence_block();
+        if (atomicAdd(&rel[st], 1) == C::NCW - 1) {
+          rel[st] = 0;
+          if (t + NSTAGE < nt && !flag[0]) {
+            issue(t + NSTAGE, st, pol);
+            atomicMax(const_cast<int*>(&flag[2]), t + NSTAGE + 1);
+          }
+        }
+      }
     }
 
     // ---- this warp's (max, sum, o) into the merge scratch ----
@@ -414,31 +413,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
           acc_o[h][j].x += __shfl_xor_sync(0xffffffffu, acc_o[h][j].x, m);
           acc_o[h][j].y += __shfl_xor_sync(0xffffffffu, acc_o[h][j].y, m);
         }
-    // (A) consumers only: every consumer has left the tile loop, so all
-    // issued copies have landed and the stages can hold the merge scratch
-    // (after an abort copies may still be in flight: write nothing).
-    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-    float* mw = merge_s + C::NCW * C::NREP_P * D;
-    float* lw = mw + C::NCW * C::NREP_P;
-    if (!flag[0] && rsub == 0)
-#pragma unroll
-      for (int h = 0; h < NREP; ++h)
-#pragma unroll
-        for (int j = 0; j < C::EPC / 2; ++j)
-          *reinterpret_cast<float2*>(merge_s + (warp * C::NREP_P + h) * D + cp * C::EPC + 2 * j) =
-              acc_o[h][j];
-    if (!flag[0] && lane < C::G)
-#pragma unroll
-      for (int i = 0; i < C::NV; ++i) {
-        mw[warp * C::NREP_P + lane * C::NV + i] = mref[i];
-        lw[warp * C::NREP_P + lane * C::NV + i] = lsum[i];
-      }
-  }
-  __syncthreads();
-  // let the merge kernel's CTAs be scheduled while this grid drains
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __syncthreads();  // every warp has left the tile loop
 
-  if (flag[0]) {  // a tile copy or a stage release did not arrive in time
+  if (flag[0]) {  // a tile copy did not arrive in time
     if (tid == 0) {
       atomicOr(p.status, GQA_DEV_WAIT_TIMEOUT);
       const int issued = flag[2];
@@ -450,6 +427,27 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR)
     __syncthreads();
     return;
   }
+  // all issued copies have landed: the stages can hold the merge scratch
+  {
+    float* mw = merge_s + C::NCW * C::NREP_P * D;
+    float* lw = mw + C::NCW * C::NREP_P;
+    if (rsub == 0)
+#pragma unroll
+      for (int h = 0; h < NREP; ++h)
+#pragma unroll
+        for (int j = 0; j < C::EPC / 2; ++j)
+          *reinterpret_cast<float2*>(merge_s + (warp * C::NREP_P + h) * D + (lane % C::LPR) * C::EPC +
+                                     2 * j) = acc_o[h][j];
+    if (lane < C::G)
+#pragma unroll
+      for (int i = 0; i < C::NV; ++i) {
+        mw[warp * C::NREP_P + lane * C::NV + i] = mref[i];
+        lw[warp * C::NREP_P + lane * C::NV + i] = lsum[i];
+      }
+  }
+  __syncthreads();
+  // let the merge kernel's CTAs be scheduled while this grid drains
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- merge the consumer warps, then write O or this split's partial ----
   const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
@@ -574,6 +572,10 @@ cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   static bool configured = false;  // per instantiation; attribute is per-function
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    // two CTAs per SM need the largest shared-memory carveout
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     configured = true;
   }

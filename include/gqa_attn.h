@@ -33,10 +33,11 @@
  *     synchronises the device.
  *   - The library allocates no device memory.  Scratch memory (the split-KV
  *     partials) is a caller-owned `workspace` whose size the matching
- *     *_workspace_size() call returns for the current device.  The workspace
- *     must be zero-filled once before its first use (e.g. cudaMemset); the
- *     library leaves it ready for the next call afterwards.  Two calls that
- *     may run concurrently on the GPU must not share a workspace.
+ *     *_workspace_size() call returns for the current device.  Only its first
+ *     4 bytes (the device status word) need to start at zero; every partial
+ *     is written before it is read within a call.  Two calls that may run
+ *     concurrently on the GPU must not share a workspace.  A decode call
+ *     that splits the keys launches two kernels (splits, then merge).
  *   - Arguments are validated on the host before any launch; on failure the
  *     call returns a negative gqa_status_t and launches nothing.
  *   - Per-request lengths that are out of range on the device are clamped
