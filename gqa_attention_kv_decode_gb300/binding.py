@@ -24,6 +24,7 @@ GQA_ERR_UNSUPPORTED = -2
 GQA_ERR_NOT_DEVICE_PTR = -3
 GQA_ERR_CUDA = -4
 GQA_ERR_WORKSPACE = -5
+GQA_ERR_SCRATCH_LIMIT = -6
 
 GQA_F32 = 0
 GQA_BF16 = 1
@@ -35,6 +36,7 @@ GQA_DEV_WAIT_TIMEOUT = 4
 EXPORTED = (
     "gqa_attn_decode_workspace_size",
     "gqa_attn_decode",
+    "gqa_attn_decode_noalloc",
     "gqa_attn_decode_q4_workspace_size",
     "gqa_attn_decode_q4",
     "gqa_attn_prefill",
@@ -70,6 +72,8 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode_workspace_size.restype = sz
     L.gqa_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
     L.gqa_attn_decode.restype = i32
+    L.gqa_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+    L.gqa_attn_decode_noalloc.restype = i32
     L.gqa_attn_decode_q4_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.gqa_attn_decode_q4_workspace_size.restype = sz
     L.gqa_attn_decode_q4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -143,6 +147,21 @@ def gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len=None, stre
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream))
     _check(rc, "gqa_attn_decode")
+
+
+def gqa_attn_decode_noalloc(q, k, v, o, kv_lens, scale, max_kv_len=None, stream=None):
+    """gqa_attn_decode without a workspace: the library's built-in scratch is
+    used (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    B, Hq, Tq, D = q.shape
+    Hkv, S_cap = k.shape[1], k.shape[2]
+    if Tq != 1:
+        raise ValueError("decode takes one query row per request")
+    if max_kv_len is None:
+        max_kv_len = S_cap
+    rc = lib().gqa_attn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(kv_lens), B, Hq, Hkv,
+                                       D, S_cap, int(max_kv_len), float(scale), _dtype_code(q),
+                                       _stream(stream))
+    _check(rc, "gqa_attn_decode_noalloc")
 
 
 def gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len) -> int:

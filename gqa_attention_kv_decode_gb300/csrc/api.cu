@@ -116,6 +116,7 @@ GQA_ATTN_API const char* gqa_attn_status_string(int status) {
     case GQA_ERR_NOT_DEVICE_PTR: return "GQA_ERR_NOT_DEVICE_PTR: a pointer is not device memory of the current device (there is no CPU path)";
     case GQA_ERR_CUDA: return "GQA_ERR_CUDA: a CUDA call or kernel launch failed";
     case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE: workspace missing or smaller than *_workspace_size()";
+    case GQA_ERR_SCRATCH_LIMIT: return "GQA_ERR_SCRATCH_LIMIT: the problem needs more scratch than the 16 MiB built into gqa_attn_decode_noalloc";
     default: return "unknown gqa_attn status";
   }
 }

@@ -62,7 +62,8 @@ typedef enum gqa_status {
   GQA_ERR_UNSUPPORTED = -2,    /* valid, but no kernel for this dtype / D        */
   GQA_ERR_NOT_DEVICE_PTR = -3, /* a pointer is not device memory                 */
   GQA_ERR_CUDA = -4,           /* a CUDA runtime call or launch failed            */
-  GQA_ERR_WORKSPACE = -5       /* workspace missing or too small                  */
+  GQA_ERR_WORKSPACE = -5,      /* workspace missing or too small                  */
+  GQA_ERR_SCRATCH_LIMIT = -6   /* problem needs more than the built-in scratch    */
 } gqa_status_t;
 
 typedef enum gqa_dtype {
@@ -104,6 +105,33 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
                                  const int32_t* kv_lens, int B, int Hq, int Hkv, int D,
                                  int S_cap, int max_kv_len, float scale, int dtype,
                                  void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-token decode without any caller-provided or allocated scratch.
+ *
+ * There is no counterpart of this entry point in the pages; it exists for
+ * callers that cannot allocate device memory (for example a runtime that only
+ * hands out the input and output buffers it owns, or code queued while its
+ * allocator is unavailable).  It computes exactly what gqa_attn_decode
+ * computes, with the same arguments minus the workspace, using a scratch array
+ * of GQA_ATTN_NOALLOC_SCRATCH_BYTES compiled into the library: every GPU that
+ * loads the library holds that array until the process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Problems whose workspace (gqa_attn_decode_workspace_size) exceeds the
+ *     array are rejected with GQA_ERR_SCRATCH_LIMIT before anything runs.
+ *   - All calls share the array.  Calls whose GPU work may overlap (other
+ *     streams, other host threads) race on it; serialise them.
+ *   - It allocates nothing and calls no allocating routine.  The device status
+ *     word of gqa_attn_decode is kept in the array and is not reported.
+ * ------------------------------------------------------------------------- */
+#define GQA_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+GQA_ATTN_API int gqa_attn_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                         const int32_t* kv_lens, int B, int Hq, int Hkv, int D,
+                                         int S_cap, int max_kv_len, float scale, int dtype,
+                                         void* stream);
 
 /* ---------------------------------------------------------------------------
  * Single-token decode over a 4-bit group-affine quantized KV cache, with the
