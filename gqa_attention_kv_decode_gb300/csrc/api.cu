@@ -192,6 +192,7 @@ GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes, const
   int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_kv_len, scale);
   if (rc != GQA_OK) return rc;
   if (group_size != 64 || D % group_size != 0) return GQA_ERR_INVALID_ARG;
+  if (S_cap % 8 != 0) return GQA_ERR_INVALID_ARG;  // scale/bias tiles are copied in 16-byte pieces
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   rc = check_ptrs({q, k_codes, v_codes, k_scale, k_bias, v_scale, v_bias, o}, dev, 16);

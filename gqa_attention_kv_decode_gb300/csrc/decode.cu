@@ -34,6 +34,7 @@
 
 #include "gqa_attn.h"
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace gqa {
@@ -53,10 +54,6 @@ struct DecodeParams {
   uint64_t wait_limit_ns;
 };
 
-__device__ __forceinline__ float load_f(const float* p) { return *p; }
-__device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-__device__ __forceinline__ void store_f(float* p, float x) { *p = x; }
-__device__ __forceinline__ void store_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 template <typename T, int D, int NREP, int R_, int NSTAGE>
 struct Cfg {
@@ -95,24 +92,6 @@ struct Cfg {
   static_assert((128 * 8 + 16) * 4 <= NSTAGE * STAGEB, "split-merge weights must fit");
   static_assert(NREP >= 1 && NREP <= 8, "at most 8 query heads per CTA");
 };
-
-// Waits for `parity` of `bar`.  Gives up (returns false) when another warp
-// has raised the abort flag, or after `limit_ns`, in which case it raises it.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
 
 template <typename T, int D, int NREP, int R_, int NSTAGE>
 __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
@@ -477,94 +456,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
   }
 }
 
-// Merges the split partials of one (request, query head) row, after the split
-// kernel has finished (programmatic dependent launch: the grid may start
-// early; griddepcontrol.wait returns once the split kernel's writes are
-// visible).  All partial loads of a thread are issued before the weights are
-// known, so the merge costs about one L2 round trip.
-//   w_s = 2^(m_s - M) / sum_s l_s 2^(m_s - M),   o = sum_s w_s o_s,   M = max_s m_s
-template <typename T, int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
-  constexpr int D4 = D / 4;
-  constexpr int NSG = 256 / D4;  // split groups: thread (sg, c4) sums splits sg, sg + NSG, ...
-  constexpr int PRE = 8;         // partials held in registers per thread
-  __shared__ float w_s[1024];
-  __shared__ float4 red[NSG][D4];
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c4 = tid % D4, sg = tid / D4;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
-  L = L < 0 ? 0 : (L > p.max_kv_len ? p.max_kv_len : L);
-  const int n_used = (L + p.chunk - 1) / p.chunk;
-  if (n_used <= 1) return;  // written by the split kernel itself
-  const float2* ml = p.ml + size_t(bh) * p.n_split;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + size_t(bh) * p.n_split * D) + c4;
-  float4 x[PRE];
-#pragma unroll
-  for (int k = 0; k < PRE; ++k) {
-    const int sidx = sg + k * NSG;
-    x[k] = sidx < n_used ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (warp == 0) {
-    float M = -INFINITY;
-    for (int sidx = lane; sidx < n_used; sidx += 32) M = fmaxf(M, __ldcg(&ml[sidx]).x);
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-    float Ls = 0.f;
-    for (int sidx = lane; sidx < n_used; sidx += 32) {
-      const float2 v = __ldcg(&ml[sidx]);
-      const float w = fast_exp2(v.x - M);
-      w_s[sidx] = w;
-      Ls += v.y * w;
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
-    const float inv = 1.f / Ls;
-    for (int sidx = lane; sidx < n_used; sidx += 32) w_s[sidx] *= inv;
-  }
-  __syncthreads();
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int k = 0; k < PRE; ++k) {
-    const int sidx = sg + k * NSG;
-    if (sidx < n_used) {
-      const float w = w_s[sidx];
-      acc.x += x[k].x * w;
-      acc.y += x[k].y * w;
-      acc.z += x[k].z * w;
-      acc.w += x[k].w * w;
-    }
-  }
-  for (int sidx = sg + PRE * NSG; sidx < n_used; sidx += NSG) {
-    const float4 v = __ldcg(po + size_t(sidx) * D4);
-    const float w = w_s[sidx];
-    acc.x += v.x * w;
-    acc.y += v.y * w;
-    acc.z += v.z * w;
-    acc.w += v.w * w;
-  }
-  red[sg][c4] = acc;
-  __syncthreads();
-  if (tid < D4) {
-    float4 t = red[0][tid];
-#pragma unroll
-    for (int k = 1; k < NSG; ++k) {
-      const float4 v = red[k][tid];
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
-    }
-    T* dst = static_cast<T*>(p.o) + size_t(bh) * D + tid * 4;
-    store_f(dst + 0, t.x);
-    store_f(dst + 1, t.y);
-    store_f(dst + 2, t.z);
-    store_f(dst + 3, t.w);
-  }
-}
-
 template <typename T, int D, int NREP, int R, int NSTAGE>
 cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   using C = Cfg<T, D, NREP, R, NSTAGE>;
@@ -581,24 +472,6 @@ cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   }
   kern<<<grid, C::NTHR, C::SMEM, stream>>>(p);
   return cudaGetLastError();
-}
-
-// The merge grid (one CTA per request and query head) is launched with
-// programmatic stream serialisation, so its launch overlaps the split
-// kernel's tail; the kernel itself waits for the split kernel's results.
-template <typename T, int D>
-cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B * p.Hq);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, p);
 }
 
 // Per (dtype, D): tile height and pipeline depth.  A stage (K + V tile) is
@@ -666,10 +539,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     e = a.D == 128 ? dispatch_nrep<__nv_bfloat16, 128>(p, grid, stream)
                    : dispatch_nrep<__nv_bfloat16, 64>(p, grid, stream);
   if (e != cudaSuccess || a.plan.n_split == 1) return e;
+  MergeParams m;
+  m.o = p.o;
+  m.kv_lens = p.kv_lens;
+  m.Hq = p.Hq;
+  m.max_kv_len = p.max_kv_len;
+  m.chunk = p.chunk;
+  m.n_split = p.n_split;
+  m.ml = p.ml;
+  m.part_o = p.part_o;
+  const int rows = a.B * a.Hq;
   if (a.dtype == GQA_F32)
-    return a.D == 128 ? launch_merge<float, 128>(p, stream) : launch_merge<float, 64>(p, stream);
-  return a.D == 128 ? launch_merge<__nv_bfloat16, 128>(p, stream)
-                    : launch_merge<__nv_bfloat16, 64>(p, stream);
+    return a.D == 128 ? launch_merge<float, 128>(m, rows, stream) : launch_merge<float, 64>(m, rows, stream);
+  return a.D == 128 ? launch_merge<__nv_bfloat16, 128>(m, rows, stream)
+                    : launch_merge<__nv_bfloat16, 64>(m, rows, stream);
 }
 
 }  // namespace gqa

@@ -65,6 +65,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits for `parity` of `bar`.  Gives up (returns false) when another warp
+// has raised the abort flag, or after `limit_ns`, in which case it raises it.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // One bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
 // from global memory into this CTA's shared memory; completion is signalled
 // as transaction bytes on `bar`.  `policy` is an L2 cache-policy descriptor.

@@ -148,7 +148,7 @@ GQA_ATTN_API int gqa_attn_decode_noalloc(const void* q, const void* k, const voi
  *            nibble of byte t, element 2t+1 in the high nibble
  *   k_scale, k_bias, v_scale, v_bias  fp16 (raw uint16 bits)
  *            [B, Hkv, S_cap, D/G]
- *   group_size  G, must be 64;  D in {64, 128}
+ *   group_size  G, must be 64;  D in {64, 128};  S_cap a multiple of 8
  *   kv_lens, max_kv_len, scale, workspace, stream: as gqa_attn_decode.
  * ------------------------------------------------------------------------- */
 GQA_ATTN_API size_t gqa_attn_decode_q4_workspace_size(int B, int Hq, int Hkv, int D,
