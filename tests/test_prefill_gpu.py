@@ -1,0 +1,105 @@
+"""Causal / chunked prefill on the tcgen05 tensor cores against the oracle.
+
+bf16 Q/K/V/O, fp32 accumulation; tolerance max abs error 2e-2.  The causal
+mask is aligned to the end of the keys: with q_len < kv_len (a chunk), query
+row i sees keys j <= i + kv_len - q_len.  For the 16,384-token case the
+oracle checks sampled rows one at a time (row i of a full causal prefill is
+a single query over keys 0..i).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_attention_kv_decode_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy()
+
+
+def case(B, Hq, Hkv, q_len, kv_len, s_cap=None, layer=0):
+    s_cap = kv_len if s_cap is None else s_cap
+    q, _, _ = inputs.qkv(B, Hq, Hkv, 64, q_len, 1, torch.bfloat16, layer=layer, device=DEV)
+    _, k, v = inputs.qkv(B, Hq, Hkv, 64, 1, s_cap, torch.bfloat16, layer=layer, device=DEV)
+    return q, k, v
+
+
+def check_full(q, k, v, kv_len, causal):
+    o = binding.prefill(q, k, v, kv_len=kv_len, causal=causal)
+    torch.cuda.synchronize()
+    ref = oracle.attention(f64(q), f64(k[:, :, :kv_len]), f64(v[:, :, :kv_len]),
+                           scale=0.125, causal=causal)["o"]
+    got = f64(o)
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= TOL, f"max abs err {err}"
+
+
+@pytest.mark.parametrize("T", [1, 5, 127, 128, 129, 300, 513])
+def test_causal_prefill_square(T):
+    q, k, v = case(1, 14, 2, T, T, layer=T)
+    check_full(q, k, v, T, True)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(1, 77), (64, 200), (129, 1000), (100, 128), (3, 300)])
+def test_chunked_prefill_aligned_to_end(q_len, kv_len):
+    q, k, v = case(1, 14, 2, q_len, kv_len, layer=q_len + kv_len)
+    check_full(q, k, v, kv_len, True)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(128, 128), (70, 300), (256, 1000)])
+def test_non_causal_prefill(q_len, kv_len):
+    q, k, v = case(1, 14, 2, q_len, kv_len, layer=7)
+    check_full(q, k, v, kv_len, False)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(2, 8, 8), (2, 32, 8), (3, 6, 1)])
+def test_prefill_head_ratios_and_batch(B, Hq, Hkv):
+    q, k, v = case(B, Hq, Hkv, 200, 333, layer=B)
+    check_full(q, k, v, 333, True)
+
+
+def test_keys_past_kv_len_are_ignored():
+    q, k, v = case(1, 14, 2, 100, 250, s_cap=300, layer=11)
+    k[:, :, 250:] = float("nan")
+    v[:, :, 250:] = float("nan")
+    check_full(q, k, v, 250, True)
+    check_full(q, k, v, 250, False)
+
+
+@pytest.mark.parametrize("T", [513, 2049, 4097])
+def test_config_causal_prefill_qwen05b(T):
+    """B=1, Hq=14, Hkv=2, D=64, bf16, q_len = kv_len = T, causal."""
+    q, k, v = case(1, 14, 2, T, T, layer=T % 13)
+    check_full(q, k, v, T, True)
+
+
+def test_config_chunked_prefill_512_at_3584():
+    """A 512-query chunk at kv offset 3584 (kv_len 4096), queries end-aligned."""
+    q, k, v = case(1, 14, 2, 512, 4096, layer=5)
+    check_full(q, k, v, 4096, True)
+
+
+def test_config_causal_prefill_16384_sampled_rows():
+    T = 16384
+    q, k, v = case(1, 14, 2, T, T, layer=3)
+    o = binding.prefill(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(T)
+    rows = sorted(set([0, 1, 127, 128, 8191, T - 1] + list(rng.integers(0, T, 10))))
+    qn, kn, vn, on = f64(q), f64(k), f64(v), f64(o)
+    for i in rows:
+        ref = oracle.attention(qn[:, :, i:i + 1], kn[:, :, :i + 1], vn[:, :, :i + 1], scale=0.125)["o"]
+        assert np.abs(on[:, :, i:i + 1] - ref).max() <= TOL, f"row {i}"
