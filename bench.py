@@ -264,6 +264,67 @@ def ragged_point(binding, B, device, stream, flush, iters=10):
     return {"B": B, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
 
 
+def q4_point(binding, S, device, stream, flush, iters=10):
+    """Hq=32, Hkv=8, D=128, B=4, 4-bit group-affine cache, 36 layer calls."""
+    B, n_layers = 4, 36
+    layers = []
+    for l in range(n_layers):
+        cache = inputs.q4_cache(B, 8, 128, S, layer=l, device=device)
+        q = inputs.randn((B, 32, 1, 128), inputs.tensor_seed(l, 0), torch.bfloat16, device)
+        layers.append((q, cache))
+    outs = [torch.empty_like(q) for q, _ in layers]
+    ws = binding.decode_q4_workspace(B, 32, 8, 128, S, device)
+
+    def step():
+        for (q, cache), o in zip(layers, outs):
+            binding.gqa_attn_decode_q4(q, *cache, o, None, 128 ** -0.5, ws, max_kv_len=S, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    ts = []
+    for _ in range(iters):
+        with torch.cuda.stream(stream):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n_layers)
+    us = statistics.median(ts)
+    nbytes = metrics.q4_decode_bytes(32, 8, 128, [S] * B)
+    del layers, outs
+    torch.cuda.empty_cache()
+    return {"S": S, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
+
+
+def prefill_point(binding, q_len, kv_len, device, stream, bf16_peak, iters=20):
+    """Hq=14, Hkv=2, D=64, bf16, causal, queries aligned to the end of the keys."""
+    q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+    k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+    v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+    o = torch.empty_like(q)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
+            e1.record(stream)
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+    flops = metrics.prefill_flops(14, 64, q_len, kv_len, causal=True)
+    tf = flops / us / 1e6
+    return {"q_len": q_len, "kv_len": kv_len, "us": round(us, 2), "TFLOPs": round(tf, 1),
+            "tokens_per_s": round(q_len / us * 1e6, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 ORACLE_SAMPLE = ("one KV head group (7 query heads, 1 of 4) of one layer call at kv_len=32768, "
@@ -486,6 +547,16 @@ def main():
         line["decode_sweep_qwen7b_28_layers"] = sweep
         line["ragged_decode_qwen3_4b_36_layers"] = [ragged_point(binding, B, device, stream, flush)
                                                    for B in (1, 2, 4, 8, 16, 64)]
+        line["q4_decode_qwen3_4b_B4_36_layers"] = [q4_point(binding, S, device, stream, flush)
+                                                  for S in (64, 2048, 16384)]
+        pf = [prefill_point(binding, T, T, device, stream, bf16_peak) for T in (513, 2049, 4097, 16384)]
+        pf.append(prefill_point(binding, 512, 4096, device, stream, bf16_peak))
+        line["prefill_causal_qwen05b_bf16"] = pf
+        big = pf[3]
+        line["roofline_prefill"] = {"bound": "tensor", "achieved": big["TFLOPs"], "peak": bf16_peak,
+                                    "unit": "TFLOP/s", "frac": big["frac_of_bf16_peak"],
+                                    "traffic": None, "kernel": "prefill_kernel (T=16384 causal)",
+                                    "peak_source": peak_src + " bf16 burst"}
         del flush
     if rank == 0:
         print(json.dumps(line), flush=True)
