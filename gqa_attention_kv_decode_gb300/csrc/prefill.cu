@@ -8,15 +8,16 @@
 // head h and reads KV head g = h / n_rep directly (no repeat_kv).  Warp roles:
 //   warp 8     TMA: Q_A, Q_B once, then K and V tiles of 128 keys (2 stages);
 //   warp 9     MMA issue (one thread): S_t = Q_t K^T (M=128, N=128, K=64) and
-//              O_t += P_t V (M=128, N=64, K=128) with tcgen05.mma, S and O in
-//              tensor memory; V is read MN-major straight from its TMA tile;
+//              O_t += P_t V (M=128, N=64, K=128) with tcgen05.mma; S, P and O
+//              live in tensor memory, V is read MN-major from its TMA tile;
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: a thread owns
-//              one query row = one TMEM lane.  Pass 1 loads the row's scores
-//              and takes the (end-aligned, causal) masked maximum; the running
-//              maximum is raised lazily (only when a tile exceeds it by more
-//              than 2^8, which also rescales O in TMEM); pass 2 reloads the
-//              scores, exponentiates and writes P (bf16) to shared memory in
-//              the 128-byte-swizzled K-major layout the tensor core reads.
+//              one query row = one TMEM lane.  In one pass over a tile it
+//              loads the row's scores, exponentiates them against the running
+//              maximum with the (end-aligned, causal) mask and writes P (bf16)
+//              back to tensor memory, where the P.V MMA reads it as its A
+//              operand.  The running maximum is raised lazily: only when a
+//              tile exceeds it by more than 2^8 does the warp rescale O in
+//              TMEM and redo that tile (the first tile takes its own maximum).
 // While one tile's softmax runs, the tensor core works on the other tile
 // (ping-pong), so MMA and exponentials overlap.  KV tiles entirely above the
 // diagonal are never loaded; tiles entirely below it are not masked.
@@ -39,20 +40,23 @@ constexpr int BN = 128;                    // keys per KV tile
 constexpr int HD = 64;                     // head dimension
 constexpr int TILE_BYTES = BM * HD * 2;    // one 128 x 64 bf16 tile: 16 KiB
 constexpr int NTHR = 320;                  // 8 softmax warps + TMA warp + MMA warp
-constexpr uint32_t TMEM_COLS = 512;        // S_A [0,128) S_B [128,256) O_A [256,320) O_B [320,384)
+constexpr uint32_t TMEM_COLS = 512;        // S_A [0,128) S_B [128,256) O_A, O_B [256,384) P_A, P_B [384,512)
 constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
 constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
 
 // shared memory (offsets from a 1024-byte aligned base)
+constexpr int NST = 4;                          // K/V stages: tiles j+1..j+3 in flight
 constexpr int OFF_Q = 0;                        // Q_A, Q_B
-constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // 2 stages
-constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;   // P_A, P_B: 2 blocks of 64 keys each
-constexpr int OFF_BAR = OFF_P + 4 * TILE_BYTES;
+constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // NST stages
+constexpr int OFF_V = OFF_K + NST * TILE_BYTES; // NST stages
+constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 // mbarrier slots
-constexpr int B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_S = 7, B_P = 9, B_O = 11, N_BARS = 13;
+constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST, B_P = B_S + 2,
+              B_O = B_P + 2, N_BARS = B_O + 2;
+static_assert(N_BARS * 8 <= 192, "barrier area");
 
 struct PrefillParams {
   __nv_bfloat16* o;
@@ -95,8 +99,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int nkv_max = max(nkv0, nkv1);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 136);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 200);
 
   if (warp == 9) {
     tmem_alloc(tslot, TMEM_COLS);
@@ -123,8 +127,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       tma_load_3d(smem + OFF_Q, &tmQ, 0, m0, b * p.Hq + h, &bars[B_Q]);
       tma_load_3d(smem + OFF_Q + TILE_BYTES, &tmQ, 0, m0 + BM, b * p.Hq + h, &bars[B_Q]);
       for (int j = 0; j < nkv_max; ++j) {
-        const int st = j & 1;
-        if (j >= 2) cta_wait(&bars[B_KE + st], uint32_t((j >> 1) - 1) & 1u, abort_flag, p.wait_limit_ns);
+        const int st = j % NST;
+        if (j >= NST) cta_wait(&bars[B_KE + st], uint32_t(j / NST - 1) & 1u, abort_flag, p.wait_limit_ns);
         if (*abort_flag) break;
         mbar_arrive_expect_tx(&bars[B_KF + st], TILE_BYTES);
         tma_load_3d(smem + OFF_K + st * TILE_BYTES, &tmK, 0, j * BN, kv_head, &bars[B_KF + st]);
@@ -137,10 +141,9 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (lane == 0) {
       const int nkv[2] = {nkv0, nkv1};
       const uint32_t q_addr = smem_u32(smem + OFF_Q);
-      const uint32_t p_addr = smem_u32(smem + OFF_P);
       auto issue_s = [&](int t, int j) {
         const uint32_t qa = q_addr + t * TILE_BYTES;
-        const uint32_t ka = smem_u32(smem + OFF_K + (j & 1) * TILE_BYTES);
+        const uint32_t ka = smem_u32(smem + OFF_K + (j % NST) * TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           mma_bf16(tmem + t * 128, sdesc_sw128(qa + kk * 32), sdesc_sw128(ka + kk * 32), IDESC_S, kk > 0);
@@ -152,26 +155,25 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int t = 0; t < 2; ++t)
         if (nkv[t] > 0) issue_s(t, 0);
       for (int j = 0; j < nkv_max; ++j) {
-        const int st = j & 1;
+        const int st = j % NST;
         bool v_ready = false, k_next = false;
         for (int t = 0; t < 2; ++t) {
           if (j >= nkv[t]) continue;
           cta_wait(&bars[B_P + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
           if (!v_ready) {
-            cta_wait(&bars[B_VF + st], uint32_t(j >> 1) & 1u, abort_flag, p.wait_limit_ns);
+            cta_wait(&bars[B_VF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
             v_ready = true;
           }
           tc_fence_after();
-          const uint32_t pa = p_addr + t * 2 * TILE_BYTES;
           const uint32_t va = smem_u32(smem + OFF_V + st * TILE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16(tmem + 256 + t * 64, sdesc_sw128(pa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32),
-                     sdesc_sw128(va + kk * 16 * 128), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk)  // P_t (bf16, TMEM) x V (MN-major, smem)
+            mma_bf16_ts(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8, sdesc_sw128(va + kk * 16 * 128),
+                        IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars[B_O + t]);
           if (j + 1 < nkv[t]) {
             if (!k_next) {
-              cta_wait(&bars[B_KF + ((j + 1) & 1)], uint32_t((j + 1) >> 1) & 1u, abort_flag, p.wait_limit_ns);
+              cta_wait(&bars[B_KF + (j + 1) % NST], uint32_t((j + 1) / NST) & 1u, abort_flag, p.wait_limit_ns);
               tc_fence_after();
               k_next = true;
             }
@@ -191,89 +193,100 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t tO = tmem + 256 + t * 64 + lane_off;
     const int qi = m0 + t * BM + r;
     const int last_key = p.causal ? min(off + qi, p.kv_len - 1) : p.kv_len - 1;
-    unsigned char* pbase = smem + OFF_P + t * 2 * TILE_BYTES;
+    const uint32_t tP = tmem + 384 + t * 64 + lane_off;
     float m_ref = -INFINITY, lsum = 0.f;
+    const float2 cc = make_float2(p.qk_scale_log2, p.qk_scale_log2);
+    // One pass over a tile: P = 2^(s*c - m_ref) (masked keys 0) written to
+    // tensor memory as bf16 pairs (the A operand of O += P V); returns the
+    // tile's sum of P and its raw score maximum.
+    auto tile_pass = [&](int n0, bool warp_masked, float2& tsum) -> float {
+      const float2 mm = make_float2(-m_ref, -m_ref);
+      float rmax = -INFINITY;
+      tsum = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[2][32];
+        tmem_ld32(tS + half * 64, sr[0]);
+        tmem_ld32(tS + half * 64 + 32, sr[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc2 = 0; cc2 < 2; ++cc2) {
+          const int c = half * 2 + cc2;
+          uint32_t pw[16];  // these 32 keys as bf16 pairs
+#pragma unroll
+          for (int e8 = 0; e8 < 4; ++e8) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = e8 * 8 + 2 * u;
+              float s0 = __uint_as_float(sr[cc2][e]), s1 = __uint_as_float(sr[cc2][e + 1]);
+              if (warp_masked) {
+                if (n0 + c * 32 + e > last_key) s0 = -INFINITY;
+                if (n0 + c * 32 + e + 1 > last_key) s1 = -INFINITY;
+              }
+              rmax = max3f(rmax, s0, s1);
+              const float2 x = ffma2(make_float2(s0, s1), cc, mm);
+              const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+              tsum = __fadd2_rn(tsum, make_float2(p0, p1));
+              const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+              pw[e8 * 4 + u] = *reinterpret_cast<const uint32_t*>(&pk);
+            }
+          }
+          tmem_st16(tP + c * 16, pw);
+        }
+      }
+      return rmax;
+    };
     for (int j = 0; j < nkv; ++j) {
       cta_wait(&bars[B_S + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
+      // P_t and O_t are free once the previous P.V of this tile is done (it
+      // was issued before this tile's S, so this wait does not stall)
+      if (j > 0) cta_wait(&bars[B_O + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
       const int n0 = j * BN;
-      const bool masked = (n0 + BN - 1 > last_key);
-      const bool warp_masked = __any_sync(0xffffffffu, masked);  // only diagonal / tail tiles
-      // pass 1: row maximum of the raw scores (the scale is positive)
-      float rmax = -INFINITY;
+      const bool warp_masked = __any_sync(0xffffffffu, n0 + BN - 1 > last_key);  // diagonal / tail
+      if (j == 0) {
+        // first tile: the reference is this tile's own maximum
+        float rmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(tS + c * 32, sr);
-        tmem_wait_ld();
-        if (!warp_masked) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) rmax = max3f(rmax, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            rmax = fmaxf(rmax, n0 + c * 32 + e > last_key ? -INFINITY : __uint_as_float(sr[e]));
-        }
-      }
-      const float tmax = rmax * p.qk_scale_log2;
-      float alpha = 1.f;
-      const bool resc = tmax > m_ref + 8.f;
-      if (resc) {
-        alpha = fast_exp2(m_ref - tmax);
-        m_ref = tmax;
-      }
-      if (j > 0) {
-        // P_t and O_t are free once the previous P.V of this tile is done
-        cta_wait(&bars[B_O + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-          uint32_t o[2][32];
-          tmem_ld32(tO, o[0]);
-          tmem_ld32(tO + 32, o[1]);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sr[2][32];
+          tmem_ld32(tS + half * 64, sr[0]);
+          tmem_ld32(tS + half * 64 + 32, sr[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int cc2 = 0; cc2 < 2; ++cc2)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[c][e] = __float_as_uint(__uint_as_float(o[c][e]) * alpha);
-          tmem_st32(tO, o[0]);
-          tmem_st32(tO + 32, o[1]);
-          tmem_wait_st();
+            for (int e = 0; e < 32; ++e) {
+              const float s = __uint_as_float(sr[cc2][e]);
+              rmax = fmaxf(rmax, (warp_masked && n0 + (half * 2 + cc2) * 32 + e > last_key) ? -INFINITY : s);
+            }
         }
+        m_ref = rmax * p.qk_scale_log2;
       }
-      lsum *= alpha;
-      // pass 2: P = 2^(s*c - m_ref) in bf16, 128-byte swizzled K-major blocks of 64 keys
-      const float2 cc = make_float2(p.qk_scale_log2, p.qk_scale_log2);
-      const float2 mm = make_float2(-m_ref, -m_ref);
-      float2 ls2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(tS + c * 32, sr);
+      float2 tsum;
+      const float tmax = tile_pass(n0, warp_masked, tsum) * p.qk_scale_log2;
+      const bool resc = tmax > m_ref + 8.f;
+      if (__any_sync(0xffffffffu, resc)) {
+        // a row's maximum rose by more than 2^8: raise its reference, rescale
+        // its O and redo the tile (whole warp, as TMEM access is warp-wide)
+        const float alpha = resc ? fast_exp2(m_ref - tmax) : 1.f;
+        if (resc) m_ref = tmax;
+        uint32_t o[2][32];
+        tmem_ld32(tO, o[0]);
+        tmem_ld32(tO + 32, o[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int e8 = 0; e8 < 4; ++e8) {
-          uint32_t w[4];
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = e8 * 8 + 2 * u;
-            const float2 x = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), cc, mm);
-            float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-            if (warp_masked) {
-              if (n0 + c * 32 + e > last_key) p0 = 0.f;
-              if (n0 + c * 32 + e + 1 > last_key) p1 = 0.f;
-            }
-            ls2 = __fadd2_rn(ls2, make_float2(p0, p1));
-            const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-            w[u] = *reinterpret_cast<const uint32_t*>(&pk);
-          }
-          const int key = c * 32 + e8 * 8;
-          const int chunk = (key & 63) >> 3;
-          unsigned char* dst = pbase + (key >> 6) * TILE_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+          for (int e = 0; e < 32; ++e) o[c][e] = __float_as_uint(__uint_as_float(o[c][e]) * alpha);
+        tmem_st32(tO, o[0]);
+        tmem_st32(tO + 32, o[1]);
+        tmem_wait_st();
+        lsum *= alpha;
+        tile_pass(n0, warp_masked, tsum);
       }
-      lsum += ls2.x + ls2.y;
-      fence_proxy_async_smem();
+      lsum += tsum.x + tsum.y;
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_P + t]);
