@@ -195,6 +195,7 @@ def sweep_point(binding, S, dtype, device, stream, flush, iters=20, graph=True):
     layers = make_layers(S, dtype, device)
     outs = [torch.empty_like(q) for q, _, _ in layers]
     ws = binding.decode_workspace(1, HQ, HKV, D, S, binding._dtype_code(layers[0][0]), device)
+    torch.cuda.synchronize()  # inputs are made on the default stream; time on `stream` only after
     with torch.cuda.stream(stream):
         for _ in range(3):
             time_decode_step(binding, layers, outs, ws, S, stream)
@@ -239,6 +240,7 @@ def ragged_point(binding, B, device, stream, flush, iters=10):
     layers = make_layers(8192, torch.bfloat16, device, n_layers=n_layers, B=B, hq=32, hkv=8)
     outs = [torch.empty_like(q) for q, _, _ in layers]
     ws = binding.decode_workspace(B, 32, 8, 128, 8192, binding.GQA_BF16, device)
+    torch.cuda.synchronize()
 
     def step():
         for (q, k, v), o in zip(layers, outs):
@@ -274,6 +276,7 @@ def q4_point(binding, S, device, stream, flush, iters=10):
         layers.append((q, cache))
     outs = [torch.empty_like(q) for q, _ in layers]
     ws = binding.decode_q4_workspace(B, 32, 8, 128, S, device)
+    torch.cuda.synchronize()
 
     def step():
         for (q, cache), o in zip(layers, outs):
@@ -305,6 +308,7 @@ def prefill_point(binding, q_len, kv_len, device, stream, bf16_peak, iters=20):
     k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
     v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
     o = torch.empty_like(q)
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(3):
             binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)

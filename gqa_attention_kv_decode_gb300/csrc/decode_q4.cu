@@ -178,21 +178,28 @@ __global__ void __launch_bounds__(Q4Cfg<D, NREP, NSTAGE>::NTHR, 2)
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t, pol);
     flag[2] = min(NSTAGE, nt);
   }
-  // q rows (scaled, fp32) and their sums over each 32-code chunk
+  // q rows (scaled, fp32), laid out so that the DSQ lanes sharing a K row
+  // read consecutive 16-byte pieces: element d = 32*c + 8*w + 4*half + j of
+  // head h sits at ((h*4 + w)*2 + half)*DSQ*4 + c*4 + j; and the sums of q
+  // over each 32-code chunk c.
+  auto qidx = [](int h, int d) {
+    const int c = d >> 5, w = (d >> 3) & 3, half = (d >> 2) & 1, j = d & 3;
+    return ((h * 4 + w) * 2 + half) * C::DSQ * 4 + c * 4 + j;
+  };
   {
     const uint32_t* qg = reinterpret_cast<const uint32_t*>(p.q + (size_t(b) * p.Hq + h0) * D);
     for (int e2 = tid; e2 < C::NREP_P * D / 2; e2 += C::NTHR) {
-      const int h = (2 * e2) / D;
+      const int h = (2 * e2) / D, d = (2 * e2) % D;
       const float2 v = h < nh ? bf16x2_to_float2(qg[e2]) : make_float2(0.f, 0.f);
-      q_s[2 * e2] = v.x * p.qscale;
-      q_s[2 * e2 + 1] = v.y * p.qscale;
+      q_s[qidx(h, d)] = v.x * p.qscale;
+      q_s[qidx(h, d + 1)] = v.y * p.qscale;
     }
   }
   __syncthreads();
   if (tid < C::NREP_P * C::DSQ) {
     const int h = tid / C::DSQ, c = tid % C::DSQ;
     float sum = 0.f;
-    for (int i = 0; i < 32; ++i) sum += q_s[h * D + 32 * c + i];
+    for (int i = 0; i < 32; ++i) sum += q_s[qidx(h, 32 * c + i)];
     qsum_s[h * C::DSQ + c] = sum;
   }
   __syncthreads();
@@ -251,8 +258,8 @@ __global__ void __launch_bounds__(Q4Cfg<D, NREP, NSTAGE>::NTHR, 2)
         }
 #pragma unroll
         for (int h = 0; h < NREP; ++h) {
-          const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + 32 * ds + 8 * w);
-          const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + 32 * ds + 8 * w + 4);
+          const float4 qa = *reinterpret_cast<const float4*>(q_s + ((h * 4 + w) * 2 + 0) * C::DSQ * 4 + ds * 4);
+          const float4 qb = *reinterpret_cast<const float4*>(q_s + ((h * 4 + w) * 2 + 1) * C::DSQ * 4 + ds * 4);
 #pragma unroll
           for (int r = 0; r < C::R; ++r) {
             acc[r][h] = ffma2(cf[r][0], make_float2(qa.x, qa.y), acc[r][h]);

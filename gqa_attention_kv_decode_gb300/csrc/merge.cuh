@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 #include "ptx.cuh"
 
@@ -132,7 +133,8 @@ cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  static const bool pdl = std::getenv("GQA_ATTN_NO_PDL") == nullptr;  // tuning switch
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, p);
 }
 
