@@ -9,6 +9,7 @@ and bf16, ragged batched decode, 4-bit decode, causal and chunked prefill) are
 measured in the same run and reported as sub-objects of the line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gqa|reference]
+    python bench.py --kernel CASE --steps K --warmup W   # one launch configuration
 
 Timing: CUDA events on the launching stream, W untimed warm-up steps, K timed
 steps bracketed by a barrier and a device synchronise; the inputs of one step
@@ -302,8 +303,12 @@ def q4_point(binding, S, device, stream, flush, iters=10):
     return {"S": S, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
 
 
-def prefill_point(binding, q_len, kv_len, device, stream, bf16_peak, iters=20):
-    """Hq=14, Hkv=2, D=64, bf16, causal, queries aligned to the end of the keys."""
+def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iters=20):
+    """Hq=14, Hkv=2, D=64, bf16, causal, queries aligned to the end of the keys.
+
+    Each timed launch follows an L2 flush on the same stream; the flush keeps
+    the device busy while the host enqueues the launch, so the events bracket
+    the kernel and not the host's launch overhead."""
     q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
     k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
     v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
@@ -317,6 +322,7 @@ def prefill_point(binding, q_len, kv_len, device, stream, bf16_peak, iters=20):
         for _ in range(iters):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            flush_l2(flush)
             e0.record(stream)
             binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
             e1.record(stream)
@@ -408,6 +414,91 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- single-kernel cases
+
+def _case_inputs(name, device):
+    """(launch, units, unit_name) for one launch configuration of the path,
+    small enough (a few hundred MB on the device) for an ncu capture."""
+    if name == "decode-f32-S32768" or name == "decode-bf16-S32768":
+        dt = torch.float32 if "f32" in name else torch.bfloat16
+        q, k, v = inputs.qkv(1, HQ, HKV, D, 1, S_HEAD, dt, device=device)
+        o = torch.empty_like(q)
+        ws = binding_mod().decode_workspace(1, HQ, HKV, D, S_HEAD, binding_mod()._dtype_code(q), device)
+        nbytes = metrics.decode_bytes(HQ, HKV, D, [S_HEAD], q.element_size())
+        return (lambda st: binding_mod().gqa_attn_decode(q, k, v, o, None, D ** -0.5, ws, max_kv_len=S_HEAD,
+                                                         stream=st)), nbytes, "bytes"
+    if name == "decode-bf16-ragged-B64":
+        lens = inputs.ragged_kv_lens(64, 64, 8192, seed=inputs.BASE_SEED + 64)
+        lens_t = torch.from_numpy(lens).to(device)
+        q, k, v = inputs.qkv(64, 32, 8, 128, 1, 8192, torch.bfloat16, device=device)
+        o = torch.empty_like(q)
+        ws = binding_mod().decode_workspace(64, 32, 8, 128, 8192, binding_mod().GQA_BF16, device)
+        nbytes = metrics.decode_bytes(32, 8, 128, lens, 2)
+        return (lambda st: binding_mod().gqa_attn_decode(q, k, v, o, lens_t, 128 ** -0.5, ws, max_kv_len=8192,
+                                                         stream=st)), nbytes, "bytes"
+    if name == "q4-B4-S16384":
+        S = 16384
+        cache = inputs.q4_cache(4, 8, 128, S, device=device)
+        q = inputs.randn((4, 32, 1, 128), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+        o = torch.empty_like(q)
+        ws = binding_mod().decode_q4_workspace(4, 32, 8, 128, S, device)
+        nbytes = metrics.q4_decode_bytes(32, 8, 128, [S] * 4)
+        return (lambda st: binding_mod().gqa_attn_decode_q4(q, *cache, o, None, 128 ** -0.5, ws, max_kv_len=S,
+                                                            stream=st)), nbytes, "bytes"
+    if name.startswith("prefill-"):
+        parts = name.split("-")[1:]           # prefill-T4097 or prefill-q512-kv4096
+        if len(parts) == 1:
+            q_len = kv_len = int(parts[0][1:])
+        else:
+            q_len, kv_len = int(parts[0][1:]), int(parts[1][2:])
+        q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+        k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+        v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+        o = torch.empty_like(q)
+        flops = metrics.prefill_flops(14, 64, q_len, kv_len, causal=True)
+        return (lambda st: binding_mod().gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, st)), flops, "flop"
+    raise SystemExit(f"unknown kernel case {name!r}")
+
+
+KERNEL_CASES = ("decode-f32-S32768", "decode-bf16-S32768", "decode-bf16-ragged-B64", "q4-B4-S16384",
+                "prefill-T4097", "prefill-T16384", "prefill-q512-kv4096")
+
+
+def binding_mod():
+    from gqa_attention_kv_decode_gb300 import binding
+    return binding
+
+
+def run_kernel_case(args):
+    """W + K launches of one configuration, each after an L2 flush, timed per
+    launch with events; prints one JSON line.  Used as the command under ncu."""
+    import __graft_entry__
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    launch, units, unit_name = _case_inputs(args.kernel, device)
+    flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+    evs = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(stream)
+            e1.record(stream)
+            if i >= args.warmup:
+                evs.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+    rate = units / us / 1e3 if unit_name == "bytes" else units / us / 1e6
+    print(json.dumps({"kernel_case": args.kernel, "us_per_launch": round(us, 3),
+                      ("GB/s" if unit_name == "bytes" else "TFLOP/s"): round(rate, 1),
+                      "algorithmic_" + unit_name: units}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -418,11 +509,15 @@ def main():
     ap.add_argument("--impl", default="gqa", choices=["gqa", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--kernel", choices=KERNEL_CASES,
+                    help="time one launch configuration only (the command profiled under ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel:
+        return run_kernel_case(args)
 
     import __graft_entry__
     from gqa_attention_kv_decode_gb300 import binding
@@ -459,22 +554,36 @@ def main():
     clocks.start()
     dist.barrier()
     torch.cuda.synchronize()
-    evs = []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for _ in range(args.steps):
-            time_decode_step(binding, layers, outs, ws, S, stream, evs)
+            time_decode_step(binding, layers, outs, ws, S, stream)
         t_end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
-    clk = clocks.stop()
     elapsed_ms = dist.max(t_start.elapsed_time(t_end))
     ms_per_step = elapsed_ms / args.steps
+
+    # the same K steps again with every layer call bracketed by events on the
+    # launching stream (kept out of the region above: an event pair between
+    # calls adds a few microseconds to each)
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            time_decode_step(binding, layers, outs, ws, S, stream, evs)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
     launch_us = [a.elapsed_time(b) * 1e3 for a, b in evs]
-    avg_launch_us = sum(launch_us) / len(launch_us)
+    isolated_call_us = sum(launch_us) / len(launch_us)
+    # calls overlap (each split kernel is launched early and prefetches while
+    # the previous merge runs), so the per-call duration is the timed region
+    # divided by its calls; an event pair around a call serialises it
+    avg_launch_us = elapsed_ms * 1e3 / (args.steps * LAYERS)
     per_launch_bytes = metrics.decode_bytes(HQ, HKV, D, [S], 4)
+    n_split = binding.gqa_attn_decode_num_splits(1, HQ, HKV, D, S, binding.GQA_F32)
+    launches_per_call = 2 if n_split > 1 else 1  # split kernel (+ merge kernel)
     achieved = per_launch_bytes / avg_launch_us / 1e3
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
 
@@ -531,11 +640,14 @@ def main():
         "hbm_fraction": round(value / world / hbm_peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                     "kernel": "decode_split_kernel<float,128,7,32,3>",
-                     "peak_source": peak_src, "avg_launch_us": round(avg_launch_us, 3)},
+                     "kernel": "decode_split_kernel<float,128,7,2,3> + decode_merge_kernel",
+                     "peak_source": peak_src, "avg_launch_us": round(avg_launch_us, 3),
+                     "timing": "events on the launching stream around the K timed steps / (K x 28 calls)",
+                     "isolated_call_us": round(isolated_call_us, 3),
+                     "n_split": n_split},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
-        "gpu_launches": len(evs),
+        "gpu_launches": LAYERS * args.steps * launches_per_call,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -553,8 +665,8 @@ def main():
                                                    for B in (1, 2, 4, 8, 16, 64)]
         line["q4_decode_qwen3_4b_B4_36_layers"] = [q4_point(binding, S, device, stream, flush)
                                                   for S in (64, 2048, 16384)]
-        pf = [prefill_point(binding, T, T, device, stream, bf16_peak) for T in (513, 2049, 4097, 16384)]
-        pf.append(prefill_point(binding, 512, 4096, device, stream, bf16_peak))
+        pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
+        pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
         line["prefill_causal_qwen05b_bf16"] = pf
         big = pf[3]
         line["roofline_prefill"] = {"bound": "tensor", "achieved": big["TFLOPs"], "peak": bf16_peak,

@@ -41,7 +41,7 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   const long target = 2L * (num_sms > 0 ? num_sms : 1);
   long chunk = ceil_div(long(max_kv_len) * units, target);
   chunk = ceil_div(chunk, tile) * tile;
-  const long lo = 2L * tile;
+  const long lo = tile;
   const long hi = (1024 / tile) * tile;
   if (chunk < lo) chunk = lo;
   if (chunk > hi) chunk = hi;

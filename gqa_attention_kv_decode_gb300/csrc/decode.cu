@@ -108,6 +108,25 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
   const int b = blockIdx.z;
   const int h0 = g * p.n_rep + hc * p.nrep_cta;
   const int nh = min(p.nrep_cta, p.n_rep - hc * p.nrep_cta);
+  const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
+  const unsigned char* kbase = static_cast<const unsigned char*>(p.k) + head_row0 * C::ROWB;
+  const unsigned char* vbase = static_cast<const unsigned char*>(p.v) + head_row0 * C::ROWB;
+
+  // This grid may have been launched while the previous one in the stream
+  // (usually the merge of the previous call) is still running.  Until
+  // grid_dependency_wait() returns nothing may be read or written; the first
+  // tiles this split will copy (assuming kv_len = max_kv_len, which only the
+  // ragged case can make wrong) are meanwhile prefetched into L2.
+  if (tid == 0 && hc == 0) {
+    for (int t = 0; t < NSTAGE; ++t) {
+      const int row0 = (split + t * p.n_split) * TILE;
+      if (row0 >= p.max_kv_len) break;
+      const uint32_t bytes = uint32_t(min(TILE, p.max_kv_len - row0)) * C::ROWB;
+      prefetch_l2_bulk(kbase + size_t(row0) * C::ROWB, bytes);
+      prefetch_l2_bulk(vbase + size_t(row0) * C::ROWB, bytes);
+    }
+  }
+  grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
   if (L < 0 || L > p.max_kv_len) {
@@ -136,10 +155,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // copy landed
   int* rel = reinterpret_cast<int*>(smem + C::OFF_BAR + NSTAGE * 8);  // warps done with a stage
   volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [2] issued
-
-  const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
-  const unsigned char* kbase = static_cast<const unsigned char*>(p.k) + head_row0 * C::ROWB;
-  const unsigned char* vbase = static_cast<const unsigned char*>(p.v) + head_row0 * C::ROWB;
 
   // Copy k-th tile of this split into stage st (one elected thread).
   auto issue = [&](int kt, int st, uint64_t pol) {
@@ -426,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
   }
   __syncthreads();
   // let the merge kernel's CTAs be scheduled while this grid drains
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_launch_dependents();
 
   // ---- merge the consumer warps, then write O or this split's partial ----
   const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
@@ -470,8 +485,7 @@ cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, C::NTHR, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::NTHR), C::SMEM, stream, p);
 }
 
 // Per (dtype, D): tile height and pipeline depth.  A stage (K + V tile) is

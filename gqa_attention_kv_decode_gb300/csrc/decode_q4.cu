@@ -116,6 +116,26 @@ __global__ void __launch_bounds__(Q4Cfg<D, NREP, NSTAGE>::NTHR, 2)
   const int b = blockIdx.z;
   const int h0 = g * p.n_rep + hc * p.nrep_cta;
   const int nh = min(p.nrep_cta, p.n_rep - hc * p.nrep_cta);
+  const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
+  const unsigned char* kc = p.kc + head_row0 * C::CB;
+  const unsigned char* vc = p.vc + head_row0 * C::CB;
+  const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.ks) + head_row0 * C::GB;
+  const unsigned char* kb = reinterpret_cast<const unsigned char*>(p.kb) + head_row0 * C::GB;
+  const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.vs) + head_row0 * C::GB;
+  const unsigned char* vb = reinterpret_cast<const unsigned char*>(p.vb) + head_row0 * C::GB;
+
+  // As in the fp32/bf16 decode kernel: while the previous grid in the stream
+  // may still run, only prefetch this split's first code tiles into L2.
+  if (tid == 0 && hc == 0) {
+    for (int t = 0; t < NSTAGE; ++t) {
+      const int row0 = (split + t * p.n_split) * TILE;
+      if (row0 >= p.max_kv_len) break;
+      const uint32_t cbytes = uint32_t(min(TILE, p.max_kv_len - row0)) * C::CB;
+      prefetch_l2_bulk(kc + size_t(row0) * C::CB, cbytes);
+      prefetch_l2_bulk(vc + size_t(row0) * C::CB, cbytes);
+    }
+  }
+  grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
   if (L < 0 || L > p.max_kv_len) {
@@ -141,14 +161,6 @@ __global__ void __launch_bounds__(Q4Cfg<D, NREP, NSTAGE>::NTHR, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   int* rel = reinterpret_cast<int*>(smem + C::OFF_BAR + NSTAGE * 8);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
-
-  const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
-  const unsigned char* kc = p.kc + head_row0 * C::CB;
-  const unsigned char* vc = p.vc + head_row0 * C::CB;
-  const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.ks) + head_row0 * C::GB;
-  const unsigned char* kb = reinterpret_cast<const unsigned char*>(p.kb) + head_row0 * C::GB;
-  const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.vs) + head_row0 * C::GB;
-  const unsigned char* vb = reinterpret_cast<const unsigned char*>(p.vb) + head_row0 * C::GB;
 
   // k-th tile of this split into stage st: codes, scales and biases of K and
   // V.  Scale/bias copies are rounded up to whole 16-byte pieces; S_cap is a
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(Q4Cfg<D, NREP, NSTAGE>::NTHR, 2)
       lw[warp * C::NREP_P + lane * C::NV + i] = lsum[i];
     }
   __syncthreads();
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_launch_dependents();
 
   const size_t ws_row = size_t(b) * p.Hq + h0;
   for (int e = tid; e < nh * D; e += C::NTHR) {
@@ -469,8 +481,7 @@ cudaError_t launch_q4_one(const Q4Params& p, dim3 grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, C::NTHR, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::NTHR), C::SMEM, stream, p);
 }
 
 constexpr int kQ4Stages = 8;

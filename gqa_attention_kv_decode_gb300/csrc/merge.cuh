@@ -7,7 +7,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 
 #include "ptx.cuh"
 
@@ -48,7 +47,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
   const int b = bh / p.Hq;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c4 = tid % D4, sg = tid / D4;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_launch_dependents();  // the next call's split kernel may start staging
+  grid_dependency_wait();
   int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
   L = L < 0 ? 0 : (L > p.max_kv_len ? p.max_kv_len : L);
   const int n_used = (L + p.chunk - 1) / p.chunk;
@@ -62,12 +62,31 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
     x[k] = sidx < n_used ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (warp == 0) {
+    // (m, l) of splits lane, lane + 32, ...: the first ML_REG of them stay in
+    // registers between the max and the weights, the rest are read twice
+    constexpr int ML_REG = 4;
+    float2 mlr[ML_REG];
     float M = -INFINITY;
-    for (int sidx = lane; sidx < n_used; sidx += 32) M = fmaxf(M, __ldcg(&ml[sidx]).x);
+#pragma unroll
+    for (int k = 0; k < ML_REG; ++k) {
+      const int sidx = lane + 32 * k;
+      mlr[k] = sidx < n_used ? __ldcg(&ml[sidx]) : make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, mlr[k].x);
+    }
+    for (int sidx = lane + 32 * ML_REG; sidx < n_used; sidx += 32) M = fmaxf(M, __ldcg(&ml[sidx]).x);
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     float Ls = 0.f;
-    for (int sidx = lane; sidx < n_used; sidx += 32) {
+#pragma unroll
+    for (int k = 0; k < ML_REG; ++k) {
+      const int sidx = lane + 32 * k;
+      if (sidx < n_used) {
+        const float w = fast_exp2(mlr[k].x - M);
+        w_s[sidx] = w;
+        Ls += mlr[k].y * w;
+      }
+    }
+    for (int sidx = lane + 32 * ML_REG; sidx < n_used; sidx += 32) {
       const float2 v = __ldcg(&ml[sidx]);
       const float w = fast_exp2(v.x - M);
       w_s[sidx] = w;
@@ -119,23 +138,30 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
   }
 }
 
-// The merge grid (one CTA per request and query head) is launched with
-// programmatic stream serialisation, so its launch overlaps the split
-// kernel's tail; the kernel itself waits for the split kernel's results.
-template <typename T, int D>
-cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
+// Launches `kern` with programmatic stream serialisation: the grid may start
+// once every CTA of the preceding grid in the stream has called
+// griddepcontrol.launch_dependents (or exited), and must itself call
+// griddepcontrol.wait before it touches memory that grid may write.
+template <typename Kern, typename Params>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Params& p) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  static const bool pdl = std::getenv("GQA_ATTN_NO_PDL") == nullptr;  // tuning switch
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, p);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// The merge grid (one CTA per request and query head) overlaps the split
+// kernel's tail; the kernel itself waits for the split kernel's results.
+template <typename T, int D>
+cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
+  return launch_pdl(decode_merge_kernel<T, D>, dim3(rows), dim3(256), 0, stream, p);
 }
 
 }  // namespace

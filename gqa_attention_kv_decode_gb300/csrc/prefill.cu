@@ -6,7 +6,7 @@
 //
 // One CTA computes two consecutive 128-row query tiles (A and B) of one query
 // head h and reads KV head g = h / n_rep directly (no repeat_kv).  Warp roles:
-//   warp 8     TMA: Q_A, Q_B once, then K and V tiles of 128 keys (2 stages);
+//   warp 8     TMA: Q_A, Q_B once, then K and V tiles of 128 keys (4 stages);
 //   warp 9     MMA issue (one thread): S_t = Q_t K^T (M=128, N=128, K=64) and
 //              O_t += P_t V (M=128, N=64, K=128) with tcgen05.mma; S, P and O
 //              live in tensor memory, V is read MN-major from its TMA tile;
@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   } else if (warp == 9) {
     // ---------------- MMA issue ----------------
     if (lane == 0) {
-      const int nkv[2] = {nkv0, nkv1};
       const uint32_t q_addr = smem_u32(smem + OFF_Q);
       auto issue_s = [&](int t, int j) {
         const uint32_t qa = q_addr + t * TILE_BYTES;
@@ -152,13 +151,15 @@ __global__ void __launch_bounds__(NTHR, 1)
       cta_wait(&bars[B_Q], 0, abort_flag, p.wait_limit_ns);
       cta_wait(&bars[B_KF], 0, abort_flag, p.wait_limit_ns);
       tc_fence_after();
-      for (int t = 0; t < 2; ++t)
-        if (nkv[t] > 0) issue_s(t, 0);
+      if (nkv0 > 0) issue_s(0, 0);
+      if (nkv1 > 0) issue_s(1, 0);
       for (int j = 0; j < nkv_max; ++j) {
         const int st = j % NST;
         bool v_ready = false, k_next = false;
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j >= nkv[t]) continue;
+          const int nkv_t = t == 0 ? nkv0 : nkv1;
+          if (j >= nkv_t) continue;
           cta_wait(&bars[B_P + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
           if (!v_ready) {
             cta_wait(&bars[B_VF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             mma_bf16_ts(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8, sdesc_sw128(va + kk * 16 * 128),
                         IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars[B_O + t]);
-          if (j + 1 < nkv[t]) {
+          if (j + 1 < nkv_t) {
             if (!k_next) {
               cta_wait(&bars[B_KF + (j + 1) % NST], uint32_t((j + 1) / NST) & 1u, abort_flag, p.wait_limit_ns);
               tc_fence_after();
@@ -204,35 +205,26 @@ __global__ void __launch_bounds__(NTHR, 1)
       float rmax = -INFINITY;
       tsum = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[2][32];
-        tmem_ld32(tS + half * 64, sr[0]);
-        tmem_ld32(tS + half * 64 + 32, sr[1]);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(tS + c * 32, sr);
         tmem_wait_ld();
+        uint32_t pw[16];  // these 32 keys as bf16 pairs
 #pragma unroll
-        for (int cc2 = 0; cc2 < 2; ++cc2) {
-          const int c = half * 2 + cc2;
-          uint32_t pw[16];  // these 32 keys as bf16 pairs
-#pragma unroll
-          for (int e8 = 0; e8 < 4; ++e8) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int e = e8 * 8 + 2 * u;
-              float s0 = __uint_as_float(sr[cc2][e]), s1 = __uint_as_float(sr[cc2][e + 1]);
-              if (warp_masked) {
-                if (n0 + c * 32 + e > last_key) s0 = -INFINITY;
-                if (n0 + c * 32 + e + 1 > last_key) s1 = -INFINITY;
-              }
-              rmax = max3f(rmax, s0, s1);
-              const float2 x = ffma2(make_float2(s0, s1), cc, mm);
-              const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-              tsum = __fadd2_rn(tsum, make_float2(p0, p1));
-              const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-              pw[e8 * 4 + u] = *reinterpret_cast<const uint32_t*>(&pk);
-            }
+        for (int u = 0; u < 16; ++u) {
+          float s0 = __uint_as_float(sr[2 * u]), s1 = __uint_as_float(sr[2 * u + 1]);
+          if (warp_masked) {
+            if (n0 + c * 32 + 2 * u > last_key) s0 = -INFINITY;
+            if (n0 + c * 32 + 2 * u + 1 > last_key) s1 = -INFINITY;
           }
-          tmem_st16(tP + c * 16, pw);
+          rmax = max3f(rmax, s0, s1);
+          const float2 x = ffma2(make_float2(s0, s1), cc, mm);
+          const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+          tsum = __fadd2_rn(tsum, make_float2(p0, p1));
+          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+          pw[u] = *reinterpret_cast<const uint32_t*>(&pk);
         }
+        tmem_st16(tP + c * 16, pw);
       }
       return rmax;
     };
@@ -271,16 +263,15 @@ __global__ void __launch_bounds__(NTHR, 1)
         // its O and redo the tile (whole warp, as TMEM access is warp-wide)
         const float alpha = resc ? fast_exp2(m_ref - tmax) : 1.f;
         if (resc) m_ref = tmax;
-        uint32_t o[2][32];
-        tmem_ld32(tO, o[0]);
-        tmem_ld32(tO + 32, o[1]);
-        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 2; ++c) {  // 32 columns at a time keeps the register count down
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c][e] = __float_as_uint(__uint_as_float(o[c][e]) * alpha);
-        tmem_st32(tO, o[0]);
-        tmem_st32(tO + 32, o[1]);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
         tmem_wait_st();
         lsum *= alpha;
         tile_pass(n0, warp_masked, tsum);
@@ -295,27 +286,26 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (nkv > 0) {
       cta_wait(&bars[B_O + t], uint32_t(nkv - 1) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
-      uint32_t o[2][32];
-      tmem_ld32(tO, o[0]);
-      tmem_ld32(tO + 32, o[1]);
-      tmem_wait_ld();
-      if (qi < p.q_len) {
-        const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD);
+      const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+        if (qi < p.q_len) {
 #pragma unroll
           for (int e8 = 0; e8 < 4; ++e8) {
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const __nv_bfloat162 pk =
-                  __floats2bfloat162_rn(__uint_as_float(o[c][e8 * 8 + 2 * u]) * inv,
-                                        __uint_as_float(o[c][e8 * 8 + 2 * u + 1]) * inv);
+              const __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(o[e8 * 8 + 2 * u]) * inv,
+                                                              __uint_as_float(o[e8 * 8 + 2 * u + 1]) * inv);
               w[u] = *reinterpret_cast<const uint32_t*>(&pk);
             }
             dst[c * 4 + e8] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        }
       }
     }
   }

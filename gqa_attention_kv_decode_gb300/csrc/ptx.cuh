@@ -95,6 +95,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
+// Brings `bytes` (multiple of 16, address 16-byte aligned) of global memory
+// into L2 without waiting for it.  A prefetch reads nothing into registers or
+// shared memory, so it may run before the kernel's inputs are final.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its writes are visible (a no-op when this grid was not
+// launched early), and let the next grid launch before this one finishes.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // L2 policy for data read exactly once (the KV stream): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
