@@ -5,22 +5,24 @@
 // of the keys, no score matrix in memory).
 //
 // One CTA computes two consecutive 128-row query tiles (A and B) of one query
-// head h and reads KV head g = h / n_rep directly (no repeat_kv).  Warp roles:
-//   warp 8     TMA: Q_A, Q_B once, then K and V tiles of 128 keys (4 stages);
-//   warp 9     MMA issue (one thread): S_t = Q_t K^T (M=128, N=128, K=64) and
-//              O_t += P_t V (M=128, N=64, K=128) with tcgen05.mma; S, P and O
-//              live in tensor memory, V is read MN-major from its TMA tile;
-//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: a thread owns
-//              one query row = one TMEM lane.  In one pass over a tile it
-//              loads the row's scores, exponentiates them against the running
-//              maximum with the (end-aligned, causal) mask and writes P (bf16)
-//              back to tensor memory, where the P.V MMA reads it as its A
-//              operand.  The running maximum is raised lazily: only when a
-//              tile exceeds it by more than 2^8 does the warp rescale O in
-//              TMEM and redo that tile (the first tile takes its own maximum).
-// While one tile's softmax runs, the tensor core works on the other tile
-// (ping-pong), so MMA and exponentials overlap.  KV tiles entirely above the
-// diagonal are never loaded; tiles entirely below it are not masked.
+// head h and reads KV head g = h / n_rep directly (no repeat_kv).  Roles:
+//   warpgroup 2, warp 8   TMA: Q_A, Q_B once, then K and V tiles of 128 keys
+//                         through 4 shared-memory stages;
+//   warpgroup 2, warp 9   MMA issue (one thread): S_t = Q_t K^T (M=128, N=128,
+//                         K=64) and O_t += P_t V (M=128, N=64, K=128), with S,
+//                         P and O in tensor memory and V read MN-major;
+//   warpgroup 0 / 1       softmax of tile A / B: a thread owns one query row
+//                         (one TMEM lane).  It loads the row's 128 scores into
+//                         registers and at once hands the S columns back, so
+//                         the tensor core computes the next S while the
+//                         exponentials of this one run.  P (bf16) goes back to
+//                         tensor memory in two halves of 64 keys, each of
+//                         which releases its half of the P.V product.
+// The running maximum is raised lazily: only when a tile's maximum exceeds it
+// by more than 2^8 is O rescaled (in TMEM).  KV tiles entirely above the
+// diagonal are never loaded; only tiles that cross it are masked.  Warpgroup
+// 2 gives registers to the softmax warpgroups (setmaxnreg), which hold a
+// whole score row.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -39,13 +41,22 @@ constexpr int BM = 128;                    // query rows per tile (TMEM lanes)
 constexpr int BN = 128;                    // keys per KV tile
 constexpr int HD = 64;                     // head dimension
 constexpr int TILE_BYTES = BM * HD * 2;    // one 128 x 64 bf16 tile: 16 KiB
-constexpr int NTHR = 320;                  // 8 softmax warps + TMA warp + MMA warp
-constexpr uint32_t TMEM_COLS = 512;        // S_A [0,128) S_B [128,256) O_A, O_B [256,384) P_A, P_B [384,512)
+constexpr int NTHR = 384;                  // three warpgroups
+// Register split.  The kernel is compiled for 384 threads x 168 registers
+// (65,536 / 384, rounded down to a multiple of 8); the shares below must not
+// add up to more: 128 x 72 + 256 x 208 = 62,464 <= 64,512.  (The MMA-issue
+// code needs about 72 registers without spilling; a softmax thread holds a
+// 128-score row.)
+constexpr int REG_CTRL = 72, REG_SOFTMAX = 208;
+static_assert(128 * REG_CTRL + 256 * REG_SOFTMAX <= NTHR * 168, "register split exceeds the launch allocation");
+// tensor memory columns: S_A [0,128) S_B [128,256) O_A [256,320) O_B [320,384) P_A [384,448) P_B [448,512)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;
 constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
 constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
 
 // shared memory (offsets from a 1024-byte aligned base)
-constexpr int NST = 4;                          // K/V stages: tiles j+1..j+3 in flight
+constexpr int NST = 4;                          // K/V stages
 constexpr int OFF_Q = 0;                        // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // NST stages
 constexpr int OFF_V = OFF_K + NST * TILE_BYTES; // NST stages
@@ -53,10 +64,14 @@ constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
-// mbarrier slots
-constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST, B_P = B_S + 2,
-              B_O = B_P + 2, N_BARS = B_O + 2;
-static_assert(N_BARS * 8 <= 192, "barrier area");
+// mbarrier slots ([t] = per query tile)
+//   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
+//   B_P0[t]  P_t keys 0..63 stored            B_P1[t]  P_t keys 64..127 stored
+//   B_O0[t]  P.V over keys 0..63 done         B_O1[t]  P.V over all keys done
+constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST, B_SC = B_S + 2,
+              B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2, N_BARS = B_O1 + 2;
+constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8;
+static_assert(OFF_ABORT + 4 <= 256, "barrier area");
 
 struct PrefillParams {
   __nv_bfloat16* o;
@@ -71,6 +86,29 @@ __device__ __forceinline__ void cta_wait(uint64_t* bar, uint32_t parity, volatil
                                          uint64_t limit_ns) {
   if (*abort_flag) return;
   if (!mbar_wait_bounded(bar, parity, limit_ns)) *abort_flag = 1;
+}
+
+template <int N>
+__device__ __forceinline__ void set_max_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void set_max_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Exponentials of 64 scores s[0..63] of one row against the reference m
+// (P = 2^(s*c - m)), packed as 32 bf16 pairs; their sum is added to acc.
+__device__ __forceinline__ void exp_half(const uint32_t* s, float2 c, float2 mm, uint32_t (&pw)[32],
+                                         float2 (&acc)[4]) {
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    const float2 x = ffma2(make_float2(__uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1])), c, mm);
+    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+    acc[u & 3] = __fadd2_rn(acc[u & 3], make_float2(p0, p1));
+    const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+    pw[u] = *reinterpret_cast<const uint32_t*>(&pk);
+  }
 }
 
 __global__ void __launch_bounds__(NTHR, 1)
@@ -99,15 +137,18 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int nkv_max = max(nkv0, nkv1);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 200);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + OFF_TSLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + OFF_ABORT);
 
   if (warp == 9) {
     tmem_alloc(tslot, TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 256) {
-    for (int i = 0; i < N_BARS; ++i) mbar_init(&bars[i], (i == B_P || i == B_P + 1) ? 4 : 1);
+    for (int i = 0; i < N_BARS; ++i) {
+      const bool per_warp = (i >= B_SC && i < B_O0);  // arrivals of the 4 softmax warps of a tile
+      mbar_init(&bars[i], per_warp ? 4 : 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmQ);
@@ -119,9 +160,10 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == 8) {
-    // ---------------- TMA ----------------
-    if (lane == 0) {
+  if (warp >= 8) {
+    set_max_regs_dec<REG_CTRL>();
+    if (warp == 8 && lane == 0) {
+      // ---------------- TMA ----------------
       const int kv_head = b * p.Hkv + g;
       mbar_arrive_expect_tx(&bars[B_Q], 2 * TILE_BYTES);
       tma_load_3d(smem + OFF_Q, &tmQ, 0, m0, b * p.Hq + h, &bars[B_Q]);
@@ -135,163 +177,160 @@ __global__ void __launch_bounds__(NTHR, 1)
         mbar_arrive_expect_tx(&bars[B_VF + st], TILE_BYTES);
         tma_load_3d(smem + OFF_V + st * TILE_BYTES, &tmV, 0, j * BN, kv_head, &bars[B_VF + st]);
       }
-    }
-  } else if (warp == 9) {
-    // ---------------- MMA issue ----------------
-    if (lane == 0) {
-      const uint32_t q_addr = smem_u32(smem + OFF_Q);
+    } else if (warp == 9) {
+      // ---------------- MMA issue ----------------
+      // The whole warp runs this loop (waits, descriptors, loop control) in
+      // step; one elected lane issues each tcgen05 instruction.
+      const uint64_t qdesc = sdesc_sw128(smem_u32(smem + OFF_Q));
+      const uint64_t kdesc = sdesc_sw128(smem_u32(smem + OFF_K));
+      const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V));
+      constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;       // descriptor units (16 B) per tile / stage
+      constexpr uint64_t K_KSTEP = 32 >> 4, V_KSTEP = 2048 >> 4;  // per 16-deep slice
+      int k_seen = -1;  // K tiles known to have landed
+      auto need_k = [&](int j) {
+        while (k_seen < j) {
+          ++k_seen;
+          cta_wait(&bars[B_KF + k_seen % NST], uint32_t(k_seen / NST) & 1u, abort_flag, p.wait_limit_ns);
+        }
+      };
       auto issue_s = [&](int t, int j) {
-        const uint32_t qa = q_addr + t * TILE_BYTES;
-        const uint32_t ka = smem_u32(smem + OFF_K + (j % NST) * TILE_BYTES);
+        const uint64_t qd = qdesc + t * TILE_STEP, kd = kdesc + (j % NST) * TILE_STEP;
+        const uint32_t d = tmem + TM_S + t * 128;
+        mma_bf16_warp(d, qd, kd, IDESC_S, 0u);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          mma_bf16(tmem + t * 128, sdesc_sw128(qa + kk * 32), sdesc_sw128(ka + kk * 32), IDESC_S, kk > 0);
-        mma_commit(&bars[B_S + t]);
+        for (int kk = 1; kk < HD / 16; ++kk) mma_bf16_warp(d, qd + kk * K_KSTEP, kd + kk * K_KSTEP, IDESC_S, 1u);
+        mma_commit_warp(&bars[B_S + t]);
       };
       cta_wait(&bars[B_Q], 0, abort_flag, p.wait_limit_ns);
-      cta_wait(&bars[B_KF], 0, abort_flag, p.wait_limit_ns);
+      need_k(0);
       tc_fence_after();
       if (nkv0 > 0) issue_s(0, 0);
       if (nkv1 > 0) issue_s(1, 0);
       for (int j = 0; j < nkv_max; ++j) {
         const int st = j % NST;
-        bool v_ready = false, k_next = false;
+        // the next S of each tile, as soon as its softmax has read this one
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int nkv_t = t == 0 ? nkv0 : nkv1;
-          if (j >= nkv_t) continue;
-          cta_wait(&bars[B_P + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
-          if (!v_ready) {
-            cta_wait(&bars[B_VF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
-            v_ready = true;
-          }
+          if (j + 1 >= (t == 0 ? nkv0 : nkv1)) continue;
+          cta_wait(&bars[B_SC + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
+          need_k(j + 1);
           tc_fence_after();
-          const uint32_t va = smem_u32(smem + OFF_V + st * TILE_BYTES);
+          issue_s(t, j + 1);
+        }
+        // O_t += P_t V, one half of the keys at a time
+        cta_wait(&bars[B_VF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
+        const uint64_t vd = vdesc + st * TILE_STEP;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)  // P_t (bf16, TMEM) x V (MN-major, smem)
-            mma_bf16_ts(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8, sdesc_sw128(va + kk * 16 * 128),
-                        IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars[B_O + t]);
-          if (j + 1 < nkv_t) {
-            if (!k_next) {
-              cta_wait(&bars[B_KF + (j + 1) % NST], uint32_t((j + 1) / NST) & 1u, abort_flag, p.wait_limit_ns);
-              tc_fence_after();
-              k_next = true;
-            }
-            issue_s(t, j + 1);
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j >= (t == 0 ? nkv0 : nkv1)) continue;
+            cta_wait(&bars[(half ? B_P1 : B_P0) + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
+            tc_fence_after();
+            const uint32_t d = tmem + TM_O + t * 64, a = tmem + TM_P + t * 64 + half * 32;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ts_warp(d, a + kk * 8, vd + (half * 4 + kk) * V_KSTEP, IDESC_O, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_warp(&bars[(half ? B_O1 : B_O0) + t]);
           }
         }
-        mma_commit(&bars[B_KE + st]);  // stage st is free once everything issued so far is done
+        mma_commit_warp(&bars[B_KE + st]);  // stage st is free once everything issued so far is done
       }
     }
   } else {
     // ---------------- softmax of tile t = warp / 4 ----------------
+    set_max_regs_inc<REG_SOFTMAX>();
     const int t = warp >> 2;
     const int nkv = t == 0 ? nkv0 : nkv1;
     const int r = tid & (BM - 1);
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + t * 128 + lane_off;
-    const uint32_t tO = tmem + 256 + t * 64 + lane_off;
+    const uint32_t tS = tmem + TM_S + t * 128 + lane_off;
+    const uint32_t tO = tmem + TM_O + t * 64 + lane_off;
+    const uint32_t tP = tmem + TM_P + t * 64 + lane_off;
     const int qi = m0 + t * BM + r;
     const int last_key = p.causal ? min(off + qi, p.kv_len - 1) : p.kv_len - 1;
-    const uint32_t tP = tmem + 384 + t * 64 + lane_off;
+    const float c = p.qk_scale_log2;  // > 0 (the scale is checked on the host)
     float m_ref = -INFINITY, lsum = 0.f;
-    const float2 cc = make_float2(p.qk_scale_log2, p.qk_scale_log2);
-    // One pass over a tile: P = 2^(s*c - m_ref) (masked keys 0) written to
-    // tensor memory as bf16 pairs (the A operand of O += P V); returns the
-    // tile's sum of P and its raw score maximum.
-    auto tile_pass = [&](int n0, bool warp_masked, float2& tsum) -> float {
-      const float2 mm = make_float2(-m_ref, -m_ref);
-      float rmax = -INFINITY;
-      tsum = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(tS + c * 32, sr);
-        tmem_wait_ld();
-        uint32_t pw[16];  // these 32 keys as bf16 pairs
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float s0 = __uint_as_float(sr[2 * u]), s1 = __uint_as_float(sr[2 * u + 1]);
-          if (warp_masked) {
-            if (n0 + c * 32 + 2 * u > last_key) s0 = -INFINITY;
-            if (n0 + c * 32 + 2 * u + 1 > last_key) s1 = -INFINITY;
-          }
-          rmax = max3f(rmax, s0, s1);
-          const float2 x = ffma2(make_float2(s0, s1), cc, mm);
-          const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-          tsum = __fadd2_rn(tsum, make_float2(p0, p1));
-          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-          pw[u] = *reinterpret_cast<const uint32_t*>(&pk);
-        }
-        tmem_st16(tP + c * 16, pw);
-      }
-      return rmax;
-    };
     for (int j = 0; j < nkv; ++j) {
       cta_wait(&bars[B_S + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
-      // P_t and O_t are free once the previous P.V of this tile is done (it
-      // was issued before this tile's S, so this wait does not stall)
-      if (j > 0) cta_wait(&bars[B_O + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
-      const int n0 = j * BN;
-      const bool warp_masked = __any_sync(0xffffffffu, n0 + BN - 1 > last_key);  // diagonal / tail
-      if (j == 0) {
-        // first tile: the reference is this tile's own maximum
-        float rmax = -INFINITY;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sr[2][32];
-          tmem_ld32(tS + half * 64, sr[0]);
-          tmem_ld32(tS + half * 64 + 32, sr[1]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int cc2 = 0; cc2 < 2; ++cc2)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float s = __uint_as_float(sr[cc2][e]);
-              rmax = fmaxf(rmax, (warp_masked && n0 + (half * 2 + cc2) * 32 + e > last_key) ? -INFINITY : s);
-            }
-        }
-        m_ref = rmax * p.qk_scale_log2;
-      }
-      float2 tsum;
-      const float tmax = tile_pass(n0, warp_masked, tsum) * p.qk_scale_log2;
-      const bool resc = tmax > m_ref + 8.f;
-      if (__any_sync(0xffffffffu, resc)) {
-        // a row's maximum rose by more than 2^8: raise its reference, rescale
-        // its O and redo the tile (whole warp, as TMEM access is warp-wide)
-        const float alpha = resc ? fast_exp2(m_ref - tmax) : 1.f;
-        if (resc) m_ref = tmax;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {  // 32 columns at a time keeps the register count down
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + c * 32, o);
-        }
-        tmem_wait_st();
-        lsum *= alpha;
-        tile_pass(n0, warp_masked, tsum);
-      }
-      lsum += tsum.x + tsum.y;
-      tmem_wait_st();
+      uint32_t s[BN];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(s));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_P + t]);
+      if (lane == 0) mbar_arrive(&bars[B_SC + t]);  // the S columns may be overwritten now
+
+      const int n0 = j * BN;
+      if (__any_sync(0xffffffffu, n0 + BN - 1 > last_key)) {  // the diagonal (or the end) crosses this tile
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+          if (n0 + e > last_key) s[e] = 0xff800000u;  // -inf
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < BN; e += 8) {
+        mx[0] = max3f(mx[0], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+        mx[1] = max3f(mx[1], __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]));
+        mx[2] = max3f(mx[2], __uint_as_float(s[e + 4]), __uint_as_float(s[e + 5]));
+        mx[3] = max3f(mx[3], __uint_as_float(s[e + 6]), __uint_as_float(s[e + 7]));
+      }
+      const float tmax = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
+      if (j == 0) {
+        m_ref = tmax;  // key 0 is visible to every row, so this is finite
+      } else {
+        const bool resc = tmax > m_ref + 8.f;
+        if (__any_sync(0xffffffffu, resc)) {
+          // a row's maximum rose by more than 2^8: raise its reference and
+          // rescale its O once the previous P.V is done (whole warp, as TMEM
+          // access is warp-wide)
+          cta_wait(&bars[B_O1 + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
+          tc_fence_after();
+          const float alpha = resc ? fast_exp2(m_ref - tmax) : 1.f;
+          if (resc) m_ref = tmax;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + cc * 32, o);
+          }
+          tmem_wait_st();
+          lsum *= alpha;
+        }
+      }
+      const float2 cc2 = make_float2(c, c), mm = make_float2(-m_ref, -m_ref);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pw[32];
+        exp_half(s + half * 64, cc2, mm, pw, acc);
+        // P_t half may be overwritten once the previous P.V has read it
+        if (j > 0) cta_wait(&bars[(half ? B_O1 : B_O0) + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
+        tc_fence_after();
+        tmem_st32(tP + half * 32, pw);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[(half ? B_P1 : B_P0) + t]);
+      }
+      lsum += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
     }
     // ---- epilogue: O / l, bf16, to global memory ----
     if (nkv > 0) {
-      cta_wait(&bars[B_O + t], uint32_t(nkv - 1) & 1u, abort_flag, p.wait_limit_ns);
+      cta_wait(&bars[B_O1 + t], uint32_t(nkv - 1) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
       const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
       uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
+        tmem_ld32(tO + cc * 32, o);
         tmem_wait_ld();
         if (qi < p.q_len) {
 #pragma unroll
@@ -303,7 +342,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                                               __uint_as_float(o[e8 * 8 + 2 * u + 1]) * inv);
               w[u] = *reinterpret_cast<const uint32_t*>(&pk);
             }
-            dst[c * 4 + e8] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[cc * 4 + e8] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
