@@ -8,9 +8,10 @@
 // head h and reads KV head g = h / n_rep directly (no repeat_kv).  Roles:
 //   warpgroup 2, warp 8   TMA: Q_A, Q_B once, then K and V tiles of 128 keys
 //                         through 4 shared-memory stages;
-//   warpgroup 2, warp 9   MMA issue (one thread): S_t = Q_t K^T (M=128, N=128,
-//                         K=64) and O_t += P_t V (M=128, N=64, K=128), with S,
-//                         P and O in tensor memory and V read MN-major;
+//   warpgroup 2, warp 9   MMA issue of S_t = Q_t K^T (M=128, N=128, K=64);
+//   warps 10, 11          MMA issue of O_t += P_t V (M=128, N=64, K=128) for
+//                         t = A, B; S, P and O live in tensor memory, V is
+//                         read MN-major from its TMA tile;
 //   warpgroup 0 / 1       softmax of tile A / B: a thread owns one query row
 //                         (one TMEM lane).  It loads the row's 128 scores into
 //                         registers and at once hands the S columns back, so
@@ -81,9 +82,11 @@ struct PrefillParams {
 };
 
 // Bounded wait shared by the whole CTA: once one thread gives up, the
-// others stop waiting too and the outputs are poisoned with NaN.
+// others stop waiting too and the outputs are poisoned with NaN.  A phase
+// that has already completed costs one probe.
 __device__ __forceinline__ void cta_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
   if (*abort_flag) return;
   if (!mbar_wait_bounded(bar, parity, limit_ns)) *abort_flag = 1;
 }
@@ -147,7 +150,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (tid == 256) {
     for (int i = 0; i < N_BARS; ++i) {
       const bool per_warp = (i >= B_SC && i < B_O0);  // arrivals of the 4 softmax warps of a tile
-      mbar_init(&bars[i], per_warp ? 4 : 1);
+      const bool stage_free = (i >= B_KE && i < B_KE + NST);  // the three MMA-issuing warps
+      mbar_init(&bars[i], per_warp ? 4 : stage_free ? 3 : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -178,63 +182,64 @@ __global__ void __launch_bounds__(NTHR, 1)
         tma_load_3d(smem + OFF_V + st * TILE_BYTES, &tmV, 0, j * BN, kv_head, &bars[B_VF + st]);
       }
     } else if (warp == 9) {
-      // ---------------- MMA issue ----------------
-      // The whole warp runs this loop (waits, descriptors, loop control) in
-      // step; one elected lane issues each tcgen05 instruction.
+      // ---------------- MMA issue: S_t = Q_t K^T ----------------
+      // Three warps issue tcgen05.mma (this one the scores, warps 10 and 11
+      // the P.V products of tiles A and B), so that no single instruction
+      // stream has to wait for all six hand-offs of an iteration.  Each runs
+      // its loop warp-wide (waits, descriptors, loop control in step) and one
+      // elected lane issues each tcgen05 instruction.
       const uint64_t qdesc = sdesc_sw128(smem_u32(smem + OFF_Q));
       const uint64_t kdesc = sdesc_sw128(smem_u32(smem + OFF_K));
-      const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V));
-      constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;       // descriptor units (16 B) per tile / stage
-      constexpr uint64_t K_KSTEP = 32 >> 4, V_KSTEP = 2048 >> 4;  // per 16-deep slice
-      int k_seen = -1;  // K tiles known to have landed
-      auto need_k = [&](int j) {
-        while (k_seen < j) {
-          ++k_seen;
-          cta_wait(&bars[B_KF + k_seen % NST], uint32_t(k_seen / NST) & 1u, abort_flag, p.wait_limit_ns);
-        }
-      };
-      auto issue_s = [&](int t, int j) {
-        const uint64_t qd = qdesc + t * TILE_STEP, kd = kdesc + (j % NST) * TILE_STEP;
-        const uint32_t d = tmem + TM_S + t * 128;
-        mma_bf16_warp(d, qd, kd, IDESC_S, 0u);
-#pragma unroll
-        for (int kk = 1; kk < HD / 16; ++kk) mma_bf16_warp(d, qd + kk * K_KSTEP, kd + kk * K_KSTEP, IDESC_S, 1u);
-        mma_commit_warp(&bars[B_S + t]);
-      };
+      constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;  // descriptor units (16 B) per tile / stage
+      constexpr uint64_t K_KSTEP = 32 >> 4;             // per 16-deep slice of the head dimension
       cta_wait(&bars[B_Q], 0, abort_flag, p.wait_limit_ns);
-      need_k(0);
-      tc_fence_after();
-      if (nkv0 > 0) issue_s(0, 0);
-      if (nkv1 > 0) issue_s(1, 0);
       for (int j = 0; j < nkv_max; ++j) {
         const int st = j % NST;
-        // the next S of each tile, as soon as its softmax has read this one
+        cta_wait(&bars[B_KF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
+        const uint64_t kd = kdesc + st * TILE_STEP;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j + 1 >= (t == 0 ? nkv0 : nkv1)) continue;
-          cta_wait(&bars[B_SC + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
-          need_k(j + 1);
+          if (j >= (t == 0 ? nkv0 : nkv1)) continue;
+          // S_t(j) overwrites S_t(j-1), which its softmax must have read
+          if (j > 0) cta_wait(&bars[B_SC + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
           tc_fence_after();
-          issue_s(t, j + 1);
+          const uint64_t qd = qdesc + t * TILE_STEP;
+          const uint32_t d = tmem + TM_S + t * 128;
+          mma_bf16_warp(d, qd, kd, IDESC_S, 0u);
+#pragma unroll
+          for (int kk = 1; kk < HD / 16; ++kk) mma_bf16_warp(d, qd + kk * K_KSTEP, kd + kk * K_KSTEP, IDESC_S, 1u);
+          mma_commit_warp(&bars[B_S + t]);
         }
-        // O_t += P_t V, one half of the keys at a time
+        mma_commit_warp(&bars[B_KE + st]);  // K of stage st is no longer needed once these are done
+      }
+    } else if (warp >= 10) {
+      // ---------------- MMA issue: O_t += P_t V, t = warp - 10 ----------------
+      const int t = warp - 10;
+      const int nkv = t == 0 ? nkv0 : nkv1;
+      const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V));
+      constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;
+      constexpr uint64_t V_KSTEP = 2048 >> 4;  // 16 keys of the MN-major V tile
+      const uint32_t d = tmem + TM_O + t * 64, a = tmem + TM_P + t * 64;
+      for (int j = 0; j < nkv_max; ++j) {
+        const int st = j % NST;
+        // Waited for even past this tile's last KV tile: the load of tile j
+        // orders this warp's arrival on B_KE[st] after the previous phase,
+        // so one warp can never arrive twice within a phase.
         cta_wait(&bars[B_VF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
-        const uint64_t vd = vdesc + st * TILE_STEP;
+        if (j < nkv) {
+          const uint64_t vd = vdesc + st * TILE_STEP;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j >= (t == 0 ? nkv0 : nkv1)) continue;
+          for (int half = 0; half < 2; ++half) {
             cta_wait(&bars[(half ? B_P1 : B_P0) + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
             tc_fence_after();
-            const uint32_t d = tmem + TM_O + t * 64, a = tmem + TM_P + t * 64 + half * 32;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ts_warp(d, a + kk * 8, vd + (half * 4 + kk) * V_KSTEP, IDESC_O, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16_ts_warp(d, a + half * 32 + kk * 8, vd + (half * 4 + kk) * V_KSTEP, IDESC_O,
+                               (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
             mma_commit_warp(&bars[(half ? B_O1 : B_O0) + t]);
           }
         }
-        mma_commit_warp(&bars[B_KE + st]);  // stage st is free once everything issued so far is done
+        mma_commit_warp(&bars[B_KE + st]);  // V of stage st is no longer needed (for this tile)
       }
     }
   } else {
