@@ -103,3 +103,15 @@ def test_config_causal_prefill_16384_sampled_rows():
     for i in rows:
         ref = oracle.attention(qn[:, :, i:i + 1], kn[:, :, :i + 1], vn[:, :, :i + 1], scale=0.125)["o"]
         assert np.abs(on[:, :, i:i + 1] - ref).max() <= TOL, f"row {i}"
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_growing_scores_force_rescales(causal):
+    """Keys whose norm grows along the sequence make later tiles' scores
+    exceed the running maximum by far more than 2^8 (in base 2), in first and
+    second halves of KV tiles alike, so every rescale path of the kernel runs."""
+    T = 1000
+    q, k, v = case(1, 14, 2, T, T, layer=21)
+    ramp = (1.0 + 6.0 * torch.arange(T, device=DEV, dtype=torch.float32) / T).view(1, 1, T, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    check_full(q, k, v, T, causal)
