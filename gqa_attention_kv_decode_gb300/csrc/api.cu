@@ -238,6 +238,8 @@ GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, v
                                   float scale, int causal, int dtype, void* stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
   if (q_len < 1 || kv_len < 1 || kv_len > S_cap || q_len > kv_len) return GQA_ERR_INVALID_ARG;
+  // grid: (B*Hq, pairs of 128-row query tiles), the second extent at most 65535
+  if (long(B) * Hq > 0x7fffffffL || (long(q_len) + 255) / 256 > 65535) return GQA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return GQA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return GQA_ERR_INVALID_ARG;

@@ -123,9 +123,12 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int pair = p.n_pairs - 1 - int(blockIdx.x);  // longest causal rows first
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
+  // Blocks start in the order of their linear index (x fastest): with the
+  // pair rank on y, the longest causal pairs of every head are scheduled
+  // first and the short ones fill in behind them.
+  const int pair = p.n_pairs - 1 - int(blockIdx.y);
+  const int h = int(blockIdx.x) % p.Hq;
+  const int b = int(blockIdx.x) / p.Hq;
   const int g = h / p.n_rep;
   const int m0 = pair * 2 * BM;
   const int off = p.kv_len - p.q_len;  // query row i sits at key position off + i
@@ -415,7 +418,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const dim3 grid(p.n_pairs, a.Hq, a.B);
+  const dim3 grid(a.B * a.Hq, p.n_pairs);
   prefill_kernel<<<grid, NTHR, SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -178,6 +178,9 @@ GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes,
  *   causal   1: key j visible to query row i iff j <= i + kv_len - q_len;
  *            0: every key j < kv_len visible
  *   dtype    GQA_BF16 (fp32 accumulation).   D == 64.
+ *   limits   q_len <= 65535 * 256, B * Hq < 2^31 (else GQA_ERR_INVALID_ARG).
+ * Errors: as for decode; a dtype / D without a kernel is GQA_ERR_UNSUPPORTED.
+ * Nothing is allocated; the call is asynchronous on `stream`.
  * ------------------------------------------------------------------------- */
 GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, void* o,
                                   int B, int Hq, int Hkv, int D, int q_len, int kv_len,
