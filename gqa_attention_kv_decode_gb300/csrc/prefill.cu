@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "gqa_attn.h"
@@ -64,6 +65,11 @@ constexpr int OFF_V = OFF_K + NST * TILE_BYTES; // NST stages
 constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+// Split-KV exchange (after the main loop, over the K/V stages): a partial row
+// is (O[64], m, l) padded to 68 floats; a unit is 32 rows of one tile; the 8
+// units of a CTA are spread over the cluster.
+constexpr int XROW = 68, XUNIT = 32 * XROW;
+static_assert(8 * XUNIT * 4 <= 2 * NST * TILE_BYTES, "exchange buffer fits in the K/V stages");
 
 // mbarrier slots ([t] = per query tile)
 //   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
@@ -77,6 +83,7 @@ static_assert(OFF_ABORT + 4 <= 256, "barrier area");
 struct PrefillParams {
   __nv_bfloat16* o;
   int Hq, Hkv, n_rep, q_len, kv_len, n_pairs, causal;
+  int kv_splits;        // CTAs of a cluster sharing one pair's KV tiles (1, 2, 4 or 8)
   float qk_scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
 };
@@ -89,6 +96,29 @@ __device__ __forceinline__ void cta_wait(uint64_t* bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return;
   if (*abort_flag) return;
   if (!mbar_wait_bounded(bar, parity, limit_ns)) *abort_flag = 1;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster executes each of these exactly
+// once per exchange (no thread skips one), so the barrier always completes.
+__device__ __forceinline__ void cluster_sync_all() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of this CTA's shared-memory location `p` in the CTA of `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ void dsmem_st4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
 }
 
 template <int N>
@@ -114,6 +144,9 @@ __device__ __forceinline__ void exp_half(const uint32_t* s, float2 c, float2 mm,
   }
 }
 
+// SPLIT: the pair's KV range is shared by a cluster of p.kv_splits CTAs
+// whose partial rows are merged through distributed shared memory.
+template <bool SPLIT>
 __global__ void __launch_bounds__(NTHR, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -126,9 +159,12 @@ __global__ void __launch_bounds__(NTHR, 1)
   // Blocks start in the order of their linear index (x fastest): with the
   // pair rank on y, the longest causal pairs of every head are scheduled
   // first and the short ones fill in behind them.
+  const int ks = SPLIT ? p.kv_splits : 1;
+  const int rank = SPLIT ? int(cluster_rank()) : 0;
   const int pair = p.n_pairs - 1 - int(blockIdx.y);
-  const int h = int(blockIdx.x) % p.Hq;
-  const int b = int(blockIdx.x) / p.Hq;
+  const int bh = int(blockIdx.x) / ks;  // a cluster = ks consecutive x
+  const int h = bh % p.Hq;
+  const int b = bh / p.Hq;
   const int g = h / p.n_rep;
   const int m0 = pair * 2 * BM;
   const int off = p.kv_len - p.q_len;  // query row i sits at key position off + i
@@ -139,8 +175,16 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (p.causal) n = min(n, (off + min(mstart + BM - 1, p.q_len - 1)) / BN + 1);
     return n;
   };
-  const int nkv0 = nkv_for(m0), nkv1 = nkv_for(m0 + BM);
-  const int nkv_max = max(nkv0, nkv1);
+  // The pair's KV tiles [0, nkv_all) are cut into ks contiguous shares; this
+  // CTA takes share `rank`, [j_lo, j_hi).  Below, j counts tiles of the share
+  // (barrier phases, stages) and j_lo + j is the tile's position in the keys.
+  const int nkv_a = nkv_for(m0), nkv_b = nkv_for(m0 + BM);
+  const int nkv_all = max(nkv_a, nkv_b);
+  const int j_lo = SPLIT ? nkv_all * rank / ks : 0;
+  const int j_hi = SPLIT ? nkv_all * (rank + 1) / ks : nkv_all;
+  const int nkv0 = SPLIT ? max(0, min(nkv_a, j_hi) - j_lo) : nkv_a;
+  const int nkv1 = SPLIT ? max(0, min(nkv_b, j_hi) - j_lo) : nkv_b;
+  const int nkv_max = j_hi - j_lo;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + OFF_TSLOT);
@@ -180,9 +224,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (j >= NST) cta_wait(&bars[B_KE + st], uint32_t(j / NST - 1) & 1u, abort_flag, p.wait_limit_ns);
         if (*abort_flag) break;
         mbar_arrive_expect_tx(&bars[B_KF + st], TILE_BYTES);
-        tma_load_3d(smem + OFF_K + st * TILE_BYTES, &tmK, 0, j * BN, kv_head, &bars[B_KF + st]);
+        tma_load_3d(smem + OFF_K + st * TILE_BYTES, &tmK, 0, (j_lo + j) * BN, kv_head, &bars[B_KF + st]);
         mbar_arrive_expect_tx(&bars[B_VF + st], TILE_BYTES);
-        tma_load_3d(smem + OFF_V + st * TILE_BYTES, &tmV, 0, j * BN, kv_head, &bars[B_VF + st]);
+        tma_load_3d(smem + OFF_V + st * TILE_BYTES, &tmV, 0, (j_lo + j) * BN, kv_head, &bars[B_VF + st]);
       }
     } else if (warp == 9) {
       // ---------------- MMA issue: S_t = Q_t K^T ----------------
@@ -245,17 +289,20 @@ __global__ void __launch_bounds__(NTHR, 1)
         mma_commit_warp(&bars[B_KE + st]);  // V of stage st is no longer needed (for this tile)
       }
     }
+    if (SPLIT) {  // the two exchange barriers of the split-KV epilogue (below)
+      cluster_sync_all();
+      cluster_sync_all();
+    }
   } else {
     // ---------------- softmax of tile t = warp / 4 ----------------
     set_max_regs_inc<REG_SOFTMAX>();
     const int t = warp >> 2;
     const int nkv = t == 0 ? nkv0 : nkv1;
-    const int r = tid & (BM - 1);
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + TM_S + t * 128 + lane_off;
     const uint32_t tO = tmem + TM_O + t * 64 + lane_off;
     const uint32_t tP = tmem + TM_P + t * 64 + lane_off;
-    const int qi = m0 + t * BM + r;
+    const int qi = m0 + t * BM + (tid & (BM - 1));
     const int last_key = p.causal ? min(off + qi, p.kv_len - 1) : p.kv_len - 1;
     const float c = p.qk_scale_log2;  // > 0 (the scale is checked on the host)
     float m_ref = -INFINITY, lsum = 0.f;
@@ -272,7 +319,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SC + t]);  // the S columns may be overwritten now
 
-      const int n0 = j * BN;
+      const int n0 = (j_lo + j) * BN;
       if (__any_sync(0xffffffffu, n0 + BN - 1 > last_key)) {  // the diagonal (or the end) crosses this tile
 #pragma unroll
         for (int e = 0; e < BN; ++e)
@@ -288,7 +335,11 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       const float tmax = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
       if (j == 0) {
-        m_ref = tmax;  // key 0 is visible to every row, so this is finite
+        // The first tile of the share.  Without a split it holds key 0, which
+        // every row sees; with one, a row may see no key of the share at all
+        // (then every later tile of the share is masked for it too): its
+        // reference stays -inf and its exponentials use 0 instead.
+        m_ref = tmax;
       } else {
         const bool resc = tmax > m_ref + 8.f;
         if (__any_sync(0xffffffffu, resc)) {
@@ -312,7 +363,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           lsum *= alpha;
         }
       }
-      const float2 cc2 = make_float2(c, c), mm = make_float2(-m_ref, -m_ref);
+      const float m_use = (SPLIT && m_ref == -INFINITY) ? 0.f : m_ref;
+      const float2 cc2 = make_float2(c, c), mm = make_float2(-m_use, -m_use);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -329,29 +381,100 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       lsum += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
     }
-    // ---- epilogue: O / l, bf16, to global memory ----
     if (nkv > 0) {
       cta_wait(&bars[B_O1 + t], uint32_t(nkv - 1) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
-      const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD);
+    }
+
+    // ---- epilogue: O / l, bf16, to global memory ----
+    if (!SPLIT) {
+      if (nkv > 0) {
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD;
+        const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tO + cc * 32, o);
-        tmem_wait_ld();
-        if (qi < p.q_len) {
+        for (int cc = 0; cc < 2; ++cc) {  // 32 columns at a time keeps the register count down
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_wait_ld();
+          if (qi < p.q_len) {
 #pragma unroll
-          for (int e8 = 0; e8 < 4; ++e8) {
-            uint32_t w[4];
+            for (int e8 = 0; e8 < 4; ++e8) {
+              uint32_t w[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(o[e8 * 8 + 2 * u]) * inv,
-                                                              __uint_as_float(o[e8 * 8 + 2 * u + 1]) * inv);
-              w[u] = *reinterpret_cast<const uint32_t*>(&pk);
+              for (int u = 0; u < 4; ++u) {
+                const __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(o[e8 * 8 + 2 * u]) * inv,
+                                                                __uint_as_float(o[e8 * 8 + 2 * u + 1]) * inv);
+                w[u] = *reinterpret_cast<const uint32_t*>(&pk);
+              }
+              reinterpret_cast<uint4*>(orow)[cc * 4 + e8] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            dst[cc * 4 + e8] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        }
+      }
+    } else {
+      // Split KV: every softmax thread sends its row's partial (O, m, l) to
+      // the CTA of the cluster that finishes this 32-row unit (unit u = warp,
+      // finished by rank u % ks, slot u / ks), which merges the ks partials
+      //   M = max m_s,  w_s = 2^(m_s - M),  O = sum w_s O_s / sum w_s l_s.
+      float* xbuf = reinterpret_cast<float*>(smem + OFF_K);  // the K/V stages are free after the loop
+      cluster_sync_all();  // every CTA of the cluster is done with its stages
+      {
+        const int dst_rank = warp % ks, slot = warp / ks;
+        const float* loc = xbuf + ((rank * (8 / ks) + slot) * 32 + lane) * XROW;
+        const uint32_t ra = dsmem_addr(loc, uint32_t(dst_rank));
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          if (nkv > 0) {
+            tmem_ld32(tO + cc * 32, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4)
+            dsmem_st4(ra + (cc * 8 + e4) * 16,
+                      make_float4(__uint_as_float(o[4 * e4]), __uint_as_float(o[4 * e4 + 1]),
+                                  __uint_as_float(o[4 * e4 + 2]), __uint_as_float(o[4 * e4 + 3])));
+        }
+        dsmem_st4(ra + 64 * 4, make_float4(m_ref, lsum, 0.f, 0.f));
+      }
+      cluster_sync_all();  // every partial has arrived
+      if (warp % ks == rank && qi < p.q_len) {
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD;
+        const int slot = warp / ks;
+        float M = -INFINITY;
+        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 64]);
+        float w_src[8], L = 0.f;
+#pragma unroll
+        for (int src = 0; src < 8; ++src) {
+          const float ms = src < ks ? xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 64] : -INFINITY;
+          w_src[src] = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
+          if (src < ks) L += xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 65] * w_src[src];
+        }
+        const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / L;
+#pragma unroll
+        for (int e8 = 0; e8 < 8; ++e8) {  // 8 output columns at a time
+          float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int src = 0; src < 8; ++src) {
+            if (src < ks) {
+              const float* row = xbuf + ((src * (8 / ks) + slot) * 32 + lane) * XROW + e8 * 8;
+              const float4 v0 = *reinterpret_cast<const float4*>(row);
+              const float4 v1 = *reinterpret_cast<const float4*>(row + 4);
+              const float w = w_src[src];
+              acc8[0] += v0.x * w; acc8[1] += v0.y * w; acc8[2] += v0.z * w; acc8[3] += v0.w * w;
+              acc8[4] += v1.x * w; acc8[5] += v1.y * w; acc8[6] += v1.z * w; acc8[7] += v1.w * w;
+            }
+          }
+          uint32_t wd[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const __nv_bfloat162 pk = __floats2bfloat162_rn(acc8[2 * u] * inv, acc8[2 * u + 1] * inv);
+            wd[u] = *reinterpret_cast<const uint32_t*>(&pk);
+          }
+          reinterpret_cast<uint4*>(orow)[e8] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
       }
     }
@@ -412,15 +535,51 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.qk_scale_log2 = float(double(a.scale) * 1.4426950408889634);
   p.wait_limit_ns = kWaitLimitNs;
+  // Split the KV range of a pair over a cluster when the pairs alone leave
+  // SMs idle: double the CTAs per pair (up to 8) while the grid stays within
+  // one wave and every share keeps at least 8 KV tiles.  (Beyond one wave a
+  // cluster has to wait for SMs of one GPC to free up together, which costs
+  // more than the split gains: T=4097 took 49 us unsplit, 68 us split in two.)
+  {
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long pairs = long(a.B) * a.Hq * p.n_pairs;
+    const int kv_tiles = (a.kv_len + BN - 1) / BN;
+    int ks = 1;
+    while (ks < 8 && pairs * ks * 2 <= sms && kv_tiles >= 8 * ks) ks *= 2;
+    if (const char* env = std::getenv("GQA_ATTN_PREFILL_KSPLIT")) {  // tuning override: 1, 2, 4 or 8
+      const int v = std::atoi(env);
+      if (v == 1 || v == 2 || v == 4 || v == 8) ks = v;
+    }
+    p.kv_splits = ks;
+  }
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const dim3 grid(a.B * a.Hq, p.n_pairs);
-  prefill_kernel<<<grid, NTHR, SMEM_BYTES, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  const dim3 grid(a.B * a.Hq * p.kv_splits, p.n_pairs);
+  if (p.kv_splits == 1) {
+    prefill_kernel<false><<<grid, NTHR, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTHR);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.kv_splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tq, tk, tv, p);
 }
 
 }  // namespace gqa
