@@ -45,6 +45,9 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   const long hi = (1024 / tile) * tile;
   if (chunk < lo) chunk = lo;
   if (chunk > hi) chunk = hi;
+  // two tiles or fewer: one CTA per head group is faster than a split plus
+  // its merge kernel
+  if (max_kv_len <= 2L * tile) chunk = ceil_div(max_kv_len, tile) * tile;
   if (const char* env = std::getenv("GQA_ATTN_SPLITS")) {
     const long n = std::atol(env);
     if (n > 0) chunk = ceil_div(ceil_div(max_kv_len, n), tile) * tile;

@@ -494,9 +494,7 @@ cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
 template <typename T, int D>
 struct TileCfg;
 template <> struct TileCfg<float, 128> { static constexpr int R = 2, NSTAGE = 3, TILE = 32; };
-template <> struct TileCfg<__nv_bfloat16, 128> { static constexpr int R = 4, NSTAGE = 3, TILE = 64; };
 template <> struct TileCfg<float, 64> { static constexpr int R = 4, NSTAGE = 3, TILE = 64; };
-template <> struct TileCfg<__nv_bfloat16, 64> { static constexpr int R = 4, NSTAGE = 4, TILE = 64; };
 
 template <typename T, int D>
 cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
@@ -516,9 +514,10 @@ cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
 
 }  // namespace
 
+// bf16 caches run on the tensor cores (decode_mma.cu), in tiles of 64 keys.
 int decode_tile_rows(int dtype, int D) {
   if (dtype == GQA_F32) return D == 128 ? TileCfg<float, 128>::TILE : TileCfg<float, 64>::TILE;
-  return D == 128 ? TileCfg<__nv_bfloat16, 128>::TILE : TileCfg<__nv_bfloat16, 64>::TILE;
+  return 64;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -546,12 +545,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
-  cudaError_t e;
-  if (a.dtype == GQA_F32)
-    e = a.D == 128 ? dispatch_nrep<float, 128>(p, grid, stream) : dispatch_nrep<float, 64>(p, grid, stream);
-  else
-    e = a.D == 128 ? dispatch_nrep<__nv_bfloat16, 128>(p, grid, stream)
-                   : dispatch_nrep<__nv_bfloat16, 64>(p, grid, stream);
+  const cudaError_t e = a.dtype == GQA_F32 ? (a.D == 128 ? dispatch_nrep<float, 128>(p, grid, stream)
+                                                          : dispatch_nrep<float, 64>(p, grid, stream))
+                                           : launch_decode_mma(a, stream);
   if (e != cudaSuccess || a.plan.n_split == 1) return e;
   MergeParams m;
   m.o = p.o;

@@ -1,0 +1,431 @@
+// decode_mma.cu -- single-token GQA decode over a bf16 KV cache with the
+// score and P.V products on the tensor cores (mma.sync m16n8k16, bf16 in,
+// fp32 accumulate) ("2x Faster Qwen2 Decode on Metal in Candle", "Why It
+// Matters": one pass over the grouped KV heads, no repeat_kv copy, no score
+// matrix in memory).
+//
+// With a bf16 cache every KV byte carries twice the multiply-adds of an fp32
+// one, and on the CUDA cores the kernel runs out of issue slots before HBM
+// runs out of bandwidth.  Here the query heads of one KV head are the M rows
+// of an m16n8k16 product (up to 8 heads; the other rows are zero):
+//   S = Q K^T   per warp: 16 keys x D dims, B fragments read with ldmatrix,
+//   O += P V    P taken straight from the score accumulators (their layout
+//               is the A-operand layout of the next product), V fragments
+//               read with ldmatrix.trans.
+// The CTA structure is the one of the CUDA-core kernel: 4 warps, tiles of 64
+// keys (warp w takes keys 16w..16w+15 of every tile), tiles dealt round-robin
+// to the splits, a per-warp online softmax in base 2, warps merged in shared
+// memory, and split partials merged by the shared merge kernel.  K and V
+// tiles arrive by tiled TMA with 128-byte swizzle (rows of 128 bytes, 16-byte
+// chunks XOR-ed with the row index), so the 8 rows an ldmatrix reads sit in 8
+// different bank groups.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "gqa_attn.h"
+#include "internal.h"
+#include "merge.cuh"
+#include "ptx.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace gqa {
+namespace {
+
+struct MmaParams {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* o;
+  const int32_t* kv_lens;
+  const unsigned char* k;  // row-contiguous cache, for the L2 prefetch of the first tiles
+  const unsigned char* v;
+  int B, Hq, Hkv, n_rep, n_hc, nrep_cta, S_cap, max_kv_len, chunk, n_split;
+  float qscale;  // scale * log2(e)
+  uint32_t* status;
+  float2* ml;
+  float* part_o;
+  uint64_t wait_limit_ns;
+};
+
+template <int D, int NSTAGE>
+struct MmaCfg {
+  static constexpr int TILE = 64;             // keys per tile
+  static constexpr int NW = 4;                // warps; warp w takes keys [16w, 16w + 16)
+  static constexpr int NTHR = 32 * NW;
+  static constexpr int HALVES = D / 64;       // 128-byte TMA boxes per key row
+  static constexpr int BOX = TILE * 128;      // one box: 64 rows x 128 bytes
+  static constexpr int TILEB = HALVES * BOX;  // K (or V) tile
+  static constexpr int STAGEB = 2 * TILEB;    // K + V
+  static constexpr int OFF_BAR = NSTAGE * STAGEB;
+  static constexpr int OFF_REL = OFF_BAR + NSTAGE * 8;
+  static constexpr int OFF_FLAG = OFF_REL + NSTAGE * 4;
+  static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + slack for the 1024-byte alignment of the boxes
+  static constexpr int KSTEPS = D / 16;       // k-steps of S = Q K^T
+  static constexpr int NT_O = D / 8;          // n-tiles of O
+  static constexpr int MERGE_FLOATS = NW * (8 * D + 16);  // per warp: O[8][D], m[8], l[8]
+  static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(MERGE_FLOATS * 4 <= NSTAGE * STAGEB, "warp-merge scratch fits in the stages");
+};
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of key row `row` inside a
+// 128-byte-swizzled box: the chunk index is XOR-ed with the row index mod 8.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D (+)= A B with A rows 8..15 zero (only 8 query heads per CTA): the A
+// registers a1, a3 of those rows are passed as zero.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int D, int NSTAGE>
+__global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const MmaParams p) {
+  using C = MmaCfg<D, NSTAGE>;
+  constexpr int TILE = C::TILE;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int split = blockIdx.x;
+  const int g = blockIdx.y / p.n_hc;
+  const int hc = blockIdx.y % p.n_hc;
+  const int b = blockIdx.z;
+  const int h0 = g * p.n_rep + hc * p.nrep_cta;
+  const int nh = min(p.nrep_cta, p.n_rep - hc * p.nrep_cta);
+  const int kv_head = b * p.Hkv + g;
+  const size_t head_row0 = size_t(kv_head) * size_t(p.S_cap);
+
+  // Launched early (programmatic dependent launch): until the wait returns,
+  // only prefetch the first tiles of this split into L2 (as if kv_len were
+  // max_kv_len) and the tensor maps.
+  if (tid == 0 && hc == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    for (int t = 0; t < NSTAGE; ++t) {
+      const int row0 = (split + t * p.n_split) * TILE;
+      if (row0 >= p.max_kv_len) break;
+      const uint32_t bytes = uint32_t(min(TILE, p.max_kv_len - row0)) * D * 2;
+      prefetch_l2_bulk(p.k + (head_row0 + row0) * D * 2, bytes);
+      prefetch_l2_bulk(p.v + (head_row0 + row0) * D * 2, bytes);
+    }
+  }
+  grid_dependency_wait();
+
+  int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
+  if (L < 0 || L > p.max_kv_len) {
+    if (split == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, GQA_DEV_KVLEN_CLAMPED);
+    L = L < 0 ? 0 : p.max_kv_len;
+  }
+  if (L == 0) {  // no visible key: the output row is zeros
+    if (split == 0) {
+      if (blockIdx.y == 0 && tid == 0) atomicOr(p.status, GQA_DEV_EMPTY_REQUEST);
+      for (int e = tid; e < nh * D; e += C::NTHR)
+        p.o[(size_t(b) * p.Hq + h0 + e / D) * D + e % D] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
+  const int n_used = (L + p.chunk - 1) / p.chunk;
+  if (split >= n_used) return;
+  const int nt_all = (L + TILE - 1) / TILE;
+  const int nt = (nt_all - split + n_used - 1) / n_used;  // tiles split, split + n_used, ...
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  int* rel = reinterpret_cast<int*>(smem + C::OFF_REL);
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [2] issued
+
+  // k-th tile of this split into stage st: K then V, each HALVES boxes of
+  // 64 keys x 64 dims.  Rows past S_cap arrive as zeros; rows in [L, S_cap)
+  // arrive as whatever the cache holds there (masked below).
+  auto issue = [&](int kt, int st) {
+    const int row0 = (split + kt * n_used) * TILE;
+    unsigned char* dst = smem + st * C::STAGEB;
+    mbar_arrive_expect_tx(&full[st], C::STAGEB);
+#pragma unroll
+    for (int hf = 0; hf < C::HALVES; ++hf)
+      tma_load_3d(dst + hf * C::BOX, &tmK, hf * 64, row0, kv_head, &full[st]);
+#pragma unroll
+    for (int hf = 0; hf < C::HALVES; ++hf)
+      tma_load_3d(dst + C::TILEB + hf * C::BOX, &tmV, hf * 64, row0, kv_head, &full[st]);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      rel[s] = 0;
+    }
+    fence_barrier_init();
+    flag[0] = 0;
+    flag[1] = 0;
+    for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t);
+    flag[2] = min(NSTAGE, nt);
+  }
+  // Q as A fragments: row = query head lane/4 (zero past nh), k = dims.
+  const int r = lane >> 2, c = lane & 3;
+  uint32_t qa[C::KSTEPS][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (size_t(b) * p.Hq + h0 + min(r, nh - 1)) * D);
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      qa[ks][0] = r < nh ? qrow[(16 * ks + 2 * c) / 2] : 0u;
+      qa[ks][1] = r < nh ? qrow[(16 * ks + 8 + 2 * c) / 2] : 0u;
+    }
+  }
+  __syncthreads();
+
+  const uint32_t sbase = smem_u32(smem);
+  const int kb = warp * 16;  // this warp's first key in every tile
+  const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+  float m_ref = -INFINITY, lsum = 0.f;  // head r; m_ref is the same on the 4 lanes of the head
+  float oacc[C::NT_O][4];
+#pragma unroll
+  for (int j = 0; j < C::NT_O; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+
+  for (int t = 0; t < nt; ++t) {
+    const int st = t % NSTAGE;
+    const bool ok = wait_or_abort(&full[st], uint32_t(t / NSTAGE) & 1u, flag, p.wait_limit_ns);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const int row0 = (split + t * n_used) * TILE;
+    const int wvalid = min(TILE, L - row0) - kb;  // valid keys among this warp's 16
+    const uint32_t kaddr = sbase + st * C::STAGEB, vaddr = kaddr + C::TILEB;
+    if (wvalid > 0) {
+      if (wvalid < 16) {
+        // V rows past kv_len may hold anything (NaN included): 0 x NaN would
+        // reach O, so those rows are zeroed (their P is 0)
+        unsigned char* vt = smem + st * C::STAGEB + C::TILEB;
+        const int nchunk = (16 - wvalid) * C::HALVES * 8;
+        for (int i = lane; i < nchunk; i += 32) {
+          const int row = kb + wvalid + i / (C::HALVES * 8), rem = i % (C::HALVES * 8);
+          *reinterpret_cast<uint4*>(vt + (rem / 8) * C::BOX + row * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // before the stage can be refilled by TMA
+        __syncwarp();
+      }
+      // ---- S = Q K^T over this warp's 16 keys (two n-tiles of 8) ----
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        const int key = kb + 8 * (mi >> 1) + rr, d = 16 * ks + 8 * (mi & 1);
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(kaddr + (d / 64) * C::BOX + swz(key, (d % 64) / 8), b00, b01, b10, b11);
+        mma_16816(sacc[0], qa[ks][0], qa[ks][1], b00, b01);
+        mma_16816(sacc[1], qa[ks][0], qa[ks][1], b10, b11);
+      }
+      // scores of head r for keys kb + {2c, 2c+1, 8+2c, 9+2c}, base 2
+      float sv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kl = 8 * (i >> 1) + 2 * c + (i & 1);
+        sv[i] = kl < wvalid ? sacc[i >> 1][i & 1] * p.qscale : -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      // lazy reference: raised only when a tile's maximum exceeds it by 2^8
+      const bool resc = mx > m_ref + 8.f;
+      if (__any_sync(0xffffffffu, resc)) {
+        const float alpha = resc ? fast_exp2(m_ref - mx) : 1.f;
+        if (resc) m_ref = mx;
+        lsum *= alpha;
+#pragma unroll
+        for (int j = 0; j < C::NT_O; ++j) {
+          oacc[j][0] *= alpha;
+          oacc[j][1] *= alpha;
+        }
+      }
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      float pv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pv[i] = fast_exp2(sv[i] - m_use);
+      lsum += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+      const uint32_t pa0 = pack_bf16(pv[0], pv[1]), pa2 = pack_bf16(pv[2], pv[3]);
+      // ---- O += P V: pairs of 8-dim n-tiles ----
+#pragma unroll
+      for (int jj = 0; jj < C::NT_O / 2; ++jj) {
+        const int key = kb + 8 * (mi & 1) + rr, d = 16 * jj + 8 * (mi >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vaddr + (d / 64) * C::BOX + swz(key, (d % 64) / 8), v0, v1, v2, v3);
+        mma_16816(oacc[2 * jj], pa0, pa2, v0, v1);
+        mma_16816(oacc[2 * jj + 1], pa0, pa2, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&rel[st], 1) == C::NW - 1) {  // the last warp done with the stage refills it
+        rel[st] = 0;
+        if (t + NSTAGE < nt && !flag[0]) {
+          issue(t + NSTAGE, st);
+          atomicMax(const_cast<int*>(&flag[2]), t + NSTAGE + 1);
+        }
+      }
+    }
+  }
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+  __syncthreads();  // every warp has left the tile loop
+
+  if (flag[0]) {  // a tile copy did not arrive in time
+    if (tid == 0) {
+      atomicOr(p.status, GQA_DEV_WAIT_TIMEOUT);
+      const int issued = flag[2];
+      for (int s = 0; s < NSTAGE && s < issued; ++s) {  // let the last copy on each stage land
+        const int u = s + ((issued - 1 - s) / NSTAGE) * NSTAGE;
+        mbar_wait_bounded(&full[s], uint32_t(u / NSTAGE) & 1u, p.wait_limit_ns);
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  // every issued copy has landed: the stages can hold the warp-merge scratch
+  float* merge_s = reinterpret_cast<float*>(smem);  // [warp][head][D]
+  float* mw = merge_s + C::NW * 8 * D;              // [warp][head] maxima
+  float* lw = mw + C::NW * 8;                       // [warp][head] sums
+#pragma unroll
+  for (int j = 0; j < C::NT_O; ++j)
+    *reinterpret_cast<float2*>(merge_s + (warp * 8 + r) * D + 8 * j + 2 * c) = make_float2(oacc[j][0], oacc[j][1]);
+  if (c == 0) {
+    mw[warp * 8 + r] = m_ref;
+    lw[warp * 8 + r] = lsum;
+  }
+  __syncthreads();
+  // let the merge kernel's CTAs be scheduled while this grid drains
+  grid_launch_dependents();
+
+  // ---- merge the warps, then write O or this split's partial ----
+  const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
+  for (int e = tid; e < nh * D; e += C::NTHR) {
+    const int h = e / D, d = e % D;
+    float M = mw[h];
+#pragma unroll
+    for (int w = 1; w < C::NW; ++w) M = fmaxf(M, mw[w * 8 + h]);
+    float lt = 0.f, sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) {
+      const float mwv = mw[w * 8 + h];
+      const float ew = mwv == -INFINITY ? 0.f : fast_exp2(mwv - M);
+      lt += lw[w * 8 + h] * ew;
+      sum += merge_s[(w * 8 + h) * D + d] * ew;
+    }
+    if (n_used == 1) {
+      p.o[(ws_row + h) * D + d] = __float2bfloat16_rn(sum / lt);
+    } else {
+      p.part_o[((ws_row + h) * p.n_split + split) * D + d] = sum;
+      if (d == 0) p.ml[(ws_row + h) * p.n_split + split] = make_float2(M, lt);
+    }
+  }
+}
+
+// Tensor maps of the K and V caches, [B*Hkv][S_cap][D] bf16 as a 3-D tensor
+// with 64-row x 64-dim boxes and 128-byte swizzle.  Encoding one costs about
+// a microsecond of host time, so the maps of recently used caches are kept
+// (keyed by base address and shape; a map holds no data, only the layout).
+struct MapEntry {
+  const void* base;
+  int D, S_cap, heads;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 128;
+
+bool kv_map(CUtensorMap* out, const void* base, int D, int S_cap, int heads) {
+  static std::mutex mu;
+  static MapEntry cache[kMapCache];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].base == base && cache[i].D == D && cache[i].S_cap == S_cap && cache[i].heads == heads) {
+      *out = cache[i].map;
+      return true;
+    }
+  CUtensorMap m;
+  if (!encode_bf16_rows(&m, base, uint64_t(D), uint64_t(S_cap), uint64_t(S_cap), uint64_t(heads), 64, 64))
+    return false;
+  MapEntry& e = cache[next];
+  e.base = base;
+  e.D = D;
+  e.S_cap = S_cap;
+  e.heads = heads;
+  e.map = m;
+  next = (next + 1) % kMapCache;
+  if (used < kMapCache) ++used;
+  *out = m;
+  return true;
+}
+
+template <int D, int NSTAGE>
+cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& p, dim3 grid,
+                       cudaStream_t stream) {
+  using C = MmaCfg<D, NSTAGE>;
+  auto kern = decode_mma_kernel<D, NSTAGE>;
+  static std::once_flag once;
+  static cudaError_t cfg_err = cudaSuccess;
+  std::call_once(once, [&] {
+    cfg_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cfg_err == cudaSuccess)  // two CTAs per SM need the largest shared-memory carveout
+      cfg_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+  });
+  if (cfg_err != cudaSuccess) return cfg_err;
+  return launch_pdl(kern, grid, dim3(C::NTHR), C::SMEM, stream, tk, tv, p);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.D != 64 && a.D != 128) return cudaErrorNotSupported;
+  CUtensorMap tk, tv;
+  const int heads = a.B * a.Hkv;
+  if (!kv_map(&tk, a.k, a.D, a.S_cap, heads) || !kv_map(&tv, a.v, a.D, a.S_cap, heads)) return cudaErrorInvalidValue;
+  MmaParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.kv_lens = a.kv_lens;
+  p.k = static_cast<const unsigned char*>(a.k);
+  p.v = static_cast<const unsigned char*>(a.v);
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.n_rep = a.Hq / a.Hkv;
+  p.n_hc = a.plan.n_hc;
+  p.nrep_cta = a.plan.nrep_cta;
+  p.S_cap = a.S_cap;
+  p.max_kv_len = a.max_kv_len;
+  p.chunk = a.plan.chunk;
+  p.n_split = a.plan.n_split;
+  p.qscale = float(double(a.scale) * 1.4426950408889634);
+  const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, a.plan.n_split, a.D);
+  unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
+  p.part_o = reinterpret_cast<float*>(ws + w.off_o);
+  p.wait_limit_ns = kWaitLimitNs;
+  const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
+  return a.D == 128 ? launch_mma<128, 3>(tk, tv, p, grid, stream) : launch_mma<64, 6>(tk, tv, p, grid, stream);
+}
+
+}  // namespace gqa

@@ -59,6 +59,7 @@ struct DecodeArgs {
 // Tile height (rows) of the decode kernel for this dtype / head size.
 int decode_tile_rows(int dtype, int D);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);  // bf16 caches (tensor cores)
 
 struct DecodeQ4Args {
   const void* q;

@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
 // once every CTA of the preceding grid in the stream has called
 // griddepcontrol.launch_dependents (or exited), and must itself call
 // griddepcontrol.wait before it touches memory that grid may write.
-template <typename Kern, typename Params>
-cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Params& p) {
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -154,7 +154,7 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // The merge grid (one CTA per request and query head) overlaps the split

@@ -35,6 +35,7 @@
 #include "gqa_attn.h"
 #include "internal.h"
 #include "tc.cuh"
+#include "tmap.cuh"
 
 namespace gqa {
 namespace {
@@ -484,35 +485,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (warp == 9) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// [heads][row_pitch rows][64] bf16 viewed as a 3-D tensor of which only the
-// first `rows` rows of each head exist; boxes of 128 rows x 64, 128-byte
-// swizzle.  Rows past `rows` (e.g. cache rows past kv_len, which may hold
-// anything) are never read: the copy fills them with zeros, so they add
-// exactly nothing to P.V.
+// Q, K, V as [heads][row_pitch rows][64] bf16 with only the first `rows` rows
+// of a head readable (cache rows past kv_len arrive as zeros and add exactly
+// nothing to P.V); 128-row x 64-column boxes.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_pitch, uint64_t heads) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {HD, rows, heads};
-  cuuint64_t strides[2] = {HD * 2, row_pitch * HD * 2};
-  cuuint32_t box[3] = {HD, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16_rows(map, base, HD, rows, row_pitch, heads, HD, 128);
 }
 
 }  // namespace
