@@ -671,7 +671,8 @@ def main():
         big = pf[3]
         line["roofline_prefill"] = {"bound": "tensor", "achieved": big["TFLOPs"], "peak": bf16_peak,
                                     "unit": "TFLOP/s", "frac": big["frac_of_bf16_peak"],
-                                    "traffic": None, "kernel": "prefill_kernel (T=16384 causal)",
+                                    "traffic": recorded_traffic("prefill.cu", "prefill_causal_T16384"),
+                                    "kernel": "prefill_kernel (T=16384 causal)",
                                     "peak_source": peak_src + " bf16 burst"}
         del flush
     if rank == 0:
