@@ -27,19 +27,21 @@ int device_sm_count() {
 static long ceil_div(long a, long b) { return (a + b - 1) / b; }
 
 // Chooses how many key splits each (request, KV head) gets so that the grid
-// covers about two CTAs per SM when requests are few and short, while a
+// covers about ctas_per_sm CTAs per SM when requests are few and short, while a
 // split stays at least two tiles long and at most 1024 rows (so the splits
 // of long, ragged requests balance across the SMs).  GQA_ATTN_SPLITS, when
 // set, forces the split count (tuning only).
-SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms) {
+SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms, int ctas_per_sm) {
   SplitPlan p;
   const int n_rep = Hq / Hkv;
   p.tile = tile;
   p.n_hc = (n_rep + 7) / 8;
   p.nrep_cta = int(ceil_div(n_rep, p.n_hc));
   const long units = long(B) * Hkv * p.n_hc;
-  const long target = 2L * (num_sms > 0 ? num_sms : 1);
-  long chunk = ceil_div(long(max_kv_len) * units, target);
+  const long target = long(ctas_per_sm > 0 ? ctas_per_sm : 1) * (num_sms > 0 ? num_sms : 1);
+  // at most target / units splits per unit, so that the grid is one wave
+  const long per_unit = target / units > 0 ? target / units : 1;
+  long chunk = ceil_div(max_kv_len, per_unit);
   chunk = ceil_div(chunk, tile) * tile;
   const long lo = tile;
   const long hi = (1024 / tile) * tile;
@@ -100,8 +102,8 @@ int check_ptrs(std::initializer_list<const void*> ptrs, int dev, size_t align) {
   return GQA_OK;
 }
 
-size_t decode_ws_size(int B, int Hq, int Hkv, int D, int max_kv_len, int tile) {
-  const SplitPlan p = plan_splits(B, Hq, Hkv, max_kv_len, tile, device_sm_count());
+size_t decode_ws_size(int B, int Hq, int Hkv, int D, int max_kv_len, int tile, int ctas_per_sm = 2) {
+  const SplitPlan p = plan_splits(B, Hq, Hkv, max_kv_len, tile, device_sm_count(), ctas_per_sm);
   return workspace_layout(B, Hq, Hkv, p.n_hc, p.n_split, D).total;
 }
 
@@ -183,7 +185,7 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
 GQA_ATTN_API size_t gqa_attn_decode_q4_workspace_size(int B, int Hq, int Hkv, int D,
                                                       int max_kv_len) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
-  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_q4_tile_rows(D));
+  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_q4_tile_rows(D), decode_q4_ctas_per_sm());
 }
 
 GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes, const uint16_t* k_scale,
@@ -227,7 +229,8 @@ GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes, const
   a.max_kv_len = max_kv_len;
   a.scale = scale;
   a.workspace = workspace;
-  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_q4_tile_rows(D), device_sm_count());
+  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_q4_tile_rows(D), device_sm_count(),
+                       decode_q4_ctas_per_sm());
   if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
     return GQA_ERR_WORKSPACE;
   const cudaError_t e = launch_decode_q4(a, static_cast<cudaStream_t>(stream));

@@ -39,7 +39,9 @@ struct SplitPlan {
   int nrep_cta; // query heads one CTA serves (<= 8)
 };
 
-SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms);
+// ctas_per_sm: how many CTAs of the kernel an SM holds at once; the grid is
+// sized for about that many per SM.
+SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms, int ctas_per_sm = 2);
 
 int device_sm_count();
 
@@ -78,6 +80,7 @@ struct DecodeQ4Args {
 };
 
 int decode_q4_tile_rows(int D);
+int decode_q4_ctas_per_sm();
 cudaError_t launch_decode_q4(const DecodeQ4Args& a, cudaStream_t stream);
 
 struct PrefillArgs {
