@@ -27,9 +27,9 @@ int device_sm_count() {
 static long ceil_div(long a, long b) { return (a + b - 1) / b; }
 
 // Chooses how many key splits each (request, KV head) gets so that the grid
-// covers about ctas_per_sm CTAs per SM when requests are few and short, while a
-// split stays at least two tiles long and at most 1024 rows (so the splits
-// of long, ragged requests balance across the SMs).  GQA_ATTN_SPLITS, when
+// covers at most ctas_per_sm CTAs per SM (one wave) when requests are few and
+// short, while a split stays at least one tile and at most 1024 rows long (so
+// the splits of long, ragged requests balance across the SMs).  GQA_ATTN_SPLITS, when
 // set, forces the split count (tuning only).
 SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms, int ctas_per_sm) {
   SplitPlan p;
@@ -39,10 +39,11 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   p.nrep_cta = int(ceil_div(n_rep, p.n_hc));
   const long units = long(B) * Hkv * p.n_hc;
   const long target = long(ctas_per_sm > 0 ? ctas_per_sm : 1) * (num_sms > 0 ? num_sms : 1);
-  // at most target / units splits per unit, so that the grid is one wave
+  // at most target / units splits per unit, so that the grid is one wave.
+  // Tiles are dealt round-robin to the splits, so the split length need not
+  // be a whole number of tiles.
   const long per_unit = target / units > 0 ? target / units : 1;
   long chunk = ceil_div(max_kv_len, per_unit);
-  chunk = ceil_div(chunk, tile) * tile;
   const long lo = tile;
   const long hi = (1024 / tile) * tile;
   if (chunk < lo) chunk = lo;
@@ -52,9 +53,10 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   if (max_kv_len <= 2L * tile) chunk = ceil_div(max_kv_len, tile) * tile;
   if (const char* env = std::getenv("GQA_ATTN_SPLITS")) {
     const long n = std::atol(env);
-    if (n > 0) chunk = ceil_div(ceil_div(max_kv_len, n), tile) * tile;
+    if (n > 0) chunk = ceil_div(max_kv_len, n);
   }
-  if (ceil_div(max_kv_len, chunk) > 1024) chunk = ceil_div(ceil_div(max_kv_len, 1024), tile) * tile;
+  if (chunk < lo) chunk = lo;
+  if (ceil_div(max_kv_len, chunk) > 1024) chunk = ceil_div(max_kv_len, 1024);
   p.chunk = int(chunk);
   p.n_split = int(ceil_div(max_kv_len, chunk));
   return p;
@@ -130,14 +132,15 @@ GQA_ATTN_API size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int D
                                                    int dtype) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return 0;
-  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_tile_rows(dtype, D));
+  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_tile_rows(dtype, D), decode_ctas_per_sm(dtype));
 }
 
 GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
                                             int dtype) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return GQA_ERR_INVALID_ARG;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
-  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count()).n_split;
+  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
+                     decode_ctas_per_sm(dtype)).n_split;
 }
 
 GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, void* o,
@@ -175,7 +178,8 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
   a.scale = scale;
   a.dtype = dtype;
   a.workspace = workspace;
-  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count());
+  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
+                       decode_ctas_per_sm(dtype));
   if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
     return GQA_ERR_WORKSPACE;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;

@@ -62,7 +62,7 @@ struct Cfg {
   static constexpr int NCH = ROWB / 16;  // 16-byte chunks per row
   static constexpr int EPC = 16 / E;     // elements per chunk
   static constexpr int NPART = EPC / 4;  // float4 pieces of q per chunk
-  static constexpr int NCW = 4;          // warps; each owns a quarter of every tile's rows
+  static constexpr int NCW = 8;          // warps; each owns an eighth of every tile's rows
   static constexpr int NWARP = NCW;
   static constexpr int NTHR = 32 * NWARP;
   static constexpr int DS = 8;           // lanes sharing a row in the score phase
@@ -94,7 +94,7 @@ struct Cfg {
 };
 
 template <typename T, int D, int NREP, int R_, int NSTAGE>
-__global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 2)
+__global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
     decode_split_kernel(const DecodeParams p) {
   using C = Cfg<T, D, NREP, R_, NSTAGE>;
   constexpr int TILE = C::TILE;
@@ -489,12 +489,14 @@ cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
 }
 
 // Per (dtype, D): tile height and pipeline depth.  A stage (K + V tile) is
-// 32 KiB for the 128-dim heads; three stages keep ~64 KiB in flight per CTA
-// and two CTAs fit on an SM.
+// 64 KiB; three stages keep 192 KiB in flight, so one CTA of 8 warps fills
+// an SM and the grid is one CTA per SM.  One large CTA per SM (rather than
+// two of 4 warps) halves the split partials the merge reads and evens out the
+// bandwidth each CTA gets, so the CTAs of a call finish closer together.
 template <typename T, int D>
 struct TileCfg;
-template <> struct TileCfg<float, 128> { static constexpr int R = 2, NSTAGE = 3, TILE = 32; };
-template <> struct TileCfg<float, 64> { static constexpr int R = 4, NSTAGE = 3, TILE = 64; };
+template <> struct TileCfg<float, 128> { static constexpr int R = 2, NSTAGE = 3, TILE = 64; };
+template <> struct TileCfg<float, 64> { static constexpr int R = 4, NSTAGE = 3, TILE = 128; };
 
 template <typename T, int D>
 cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
@@ -514,7 +516,10 @@ cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
 
 }  // namespace
 
-// bf16 caches run on the tensor cores (decode_mma.cu), in tiles of 64 keys.
+// bf16 caches run on the tensor cores (decode_mma.cu), in tiles of 64 keys,
+// two CTAs per SM.
+int decode_ctas_per_sm(int dtype) { return dtype == GQA_F32 ? 1 : 2; }
+
 int decode_tile_rows(int dtype, int D) {
   if (dtype == GQA_F32) return D == 128 ? TileCfg<float, 128>::TILE : TileCfg<float, 64>::TILE;
   return 64;

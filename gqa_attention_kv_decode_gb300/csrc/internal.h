@@ -58,8 +58,10 @@ struct DecodeArgs {
   SplitPlan plan;
 };
 
-// Tile height (rows) of the decode kernel for this dtype / head size.
+// Tile height (rows) of the decode kernel for this dtype / head size, and how
+// many of its CTAs an SM holds.
 int decode_tile_rows(int dtype, int D);
+int decode_ctas_per_sm(int dtype);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);  // bf16 caches (tensor cores)
 

@@ -33,19 +33,23 @@ struct MergeParams {
 // Merges the split partials of one (request, query head) row, after the split
 // kernel has finished (programmatic dependent launch: the grid may start
 // early; griddepcontrol.wait returns once the split kernel's writes are
-// visible).  All partial loads of a thread are issued before the weights are
-// known, so the merge costs about one L2 round trip.
-//   w_s = 2^(m_s - M) / sum_s l_s 2^(m_s - M),   o = sum_s w_s o_s,   M = max_s m_s
+// visible).  Thread (sg, c4) owns columns 4c4..4c4+3 of splits sg, sg + NSG,
+// ...; it loads their partials and (m, l) pairs in one round trip and
+// combines them online (running maximum), so no block-wide maximum is needed
+// before the sums.  One barrier later, NSG per-thread states per column are
+// combined with the log-sum-exp rule:
+//   M = max_s m_s,   o = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
+// The summation order is fixed, so the result is deterministic.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) {
   constexpr int D4 = D / 4;
-  constexpr int NSG = 256 / D4;  // split groups: thread (sg, c4) sums splits sg, sg + NSG, ...
-  constexpr int PRE = 8;         // partials held in registers per thread
-  __shared__ float w_s[1024];
-  __shared__ float4 red[NSG][D4];
+  constexpr int NSG = 256 / D4;  // split groups: thread (sg, c4) takes splits sg, sg + NSG, ...
+  constexpr int PRE = 8;         // partials per thread loaded before any is used
+  __shared__ float4 red_o[NSG][D4];
+  __shared__ float2 red_ml[NSG];
   const int bh = blockIdx.x;
   const int b = bh / p.Hq;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int c4 = tid % D4, sg = tid / D4;
   grid_launch_dependents();  // the next call's split kernel may start staging
   grid_dependency_wait();
@@ -56,85 +60,74 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
   const float2* ml = p.ml + size_t(bh) * p.n_split;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + size_t(bh) * p.n_split * D) + c4;
   float4 x[PRE];
+  float2 mlv[PRE];
 #pragma unroll
   for (int k = 0; k < PRE; ++k) {
     const int sidx = sg + k * NSG;
-    x[k] = sidx < n_used ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool in = sidx < n_used;
+    x[k] = in ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    mlv[k] = in ? __ldcg(&ml[sidx]) : make_float2(-INFINITY, 0.f);
   }
-  if (warp == 0) {
-    // (m, l) of splits lane, lane + 32, ...: the first ML_REG of them stay in
-    // registers between the max and the weights, the rest are read twice
-    constexpr int ML_REG = 4;
-    float2 mlr[ML_REG];
-    float M = -INFINITY;
+  float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < ML_REG; ++k) {
-      const int sidx = lane + 32 * k;
-      mlr[k] = sidx < n_used ? __ldcg(&ml[sidx]) : make_float2(-INFINITY, 0.f);
-      M = fmaxf(M, mlr[k].x);
-    }
-    for (int sidx = lane + 32 * ML_REG; sidx < n_used; sidx += 32) M = fmaxf(M, __ldcg(&ml[sidx]).x);
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-    float Ls = 0.f;
-#pragma unroll
-    for (int k = 0; k < ML_REG; ++k) {
-      const int sidx = lane + 32 * k;
-      if (sidx < n_used) {
-        const float w = fast_exp2(mlr[k].x - M);
-        w_s[sidx] = w;
-        Ls += mlr[k].y * w;
-      }
-    }
-    for (int sidx = lane + 32 * ML_REG; sidx < n_used; sidx += 32) {
-      const float2 v = __ldcg(&ml[sidx]);
-      const float w = fast_exp2(v.x - M);
-      w_s[sidx] = w;
-      Ls += v.y * w;
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
-    const float inv = 1.f / Ls;
-    for (int sidx = lane; sidx < n_used; sidx += 32) w_s[sidx] *= inv;
-  }
-  __syncthreads();
+  for (int k = 0; k < PRE; ++k) M = fmaxf(M, mlv[k].x);
+  float Ls = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int k = 0; k < PRE; ++k) {
-    const int sidx = sg + k * NSG;
-    if (sidx < n_used) {
-      const float w = w_s[sidx];
-      acc.x += x[k].x * w;
-      acc.y += x[k].y * w;
-      acc.z += x[k].z * w;
-      acc.w += x[k].w * w;
-    }
+    const float w = mlv[k].x == -INFINITY ? 0.f : fast_exp2(mlv[k].x - M);
+    Ls += mlv[k].y * w;
+    acc.x += x[k].x * w;
+    acc.y += x[k].y * w;
+    acc.z += x[k].z * w;
+    acc.w += x[k].w * w;
   }
+  // more splits than PRE * NSG: one at a time, raising the maximum as needed
   for (int sidx = sg + PRE * NSG; sidx < n_used; sidx += NSG) {
     const float4 v = __ldcg(po + size_t(sidx) * D4);
-    const float w = w_s[sidx];
+    const float2 m = __ldcg(&ml[sidx]);
+    if (m.x > M) {
+      const float a = M == -INFINITY ? 0.f : fast_exp2(M - m.x);
+      Ls *= a;
+      acc.x *= a;
+      acc.y *= a;
+      acc.z *= a;
+      acc.w *= a;
+      M = m.x;
+    }
+    const float w = fast_exp2(m.x - M);
+    Ls += m.y * w;
     acc.x += v.x * w;
     acc.y += v.y * w;
     acc.z += v.z * w;
     acc.w += v.w * w;
   }
-  red[sg][c4] = acc;
+  red_o[sg][c4] = acc;
+  if (c4 == 0) red_ml[sg] = make_float2(M, Ls);
   __syncthreads();
   if (tid < D4) {
-    float4 t = red[0][tid];
+    float Mg = red_ml[0].x;
 #pragma unroll
-    for (int k = 1; k < NSG; ++k) {
-      const float4 v = red[k][tid];
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
+    for (int k = 1; k < NSG; ++k) Mg = fmaxf(Mg, red_ml[k].x);
+    float den = 0.f;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < NSG; ++k) {
+      const float2 mk = red_ml[k];
+      const float w = mk.x == -INFINITY ? 0.f : fast_exp2(mk.x - Mg);
+      const float4 v = red_o[k][tid];
+      den += mk.y * w;
+      t.x += v.x * w;
+      t.y += v.y * w;
+      t.z += v.z * w;
+      t.w += v.w * w;
     }
+    const float inv = 1.f / den;
     T* dst = static_cast<T*>(p.o) + size_t(bh) * D + tid * 4;
-    store_f(dst + 0, t.x);
-    store_f(dst + 1, t.y);
-    store_f(dst + 2, t.z);
-    store_f(dst + 3, t.w);
+    store_f(dst + 0, t.x * inv);
+    store_f(dst + 1, t.y * inv);
+    store_f(dst + 2, t.z * inv);
+    store_f(dst + 3, t.w * inv);
   }
 }
 
