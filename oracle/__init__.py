@@ -12,4 +12,7 @@ from .gqa_oracle import (  # noqa: F401
     attention,
     dequant_q4,
     attention_q4,
+    paged_to_contiguous,
+    append_paged,
+    attention_paged,
 )

@@ -32,7 +32,12 @@ design notes):
     ("Batching Decode Attention Across Requests ...", VeloxQuant-MLX blog,
     sections "The setup" and "Part 4: the other half of the lever actually
     works": the fused kernel reads the group-affine codes, the baseline
-    dequantises them and calls SDPA -- this module is that baseline).
+    dequantises them and calls SDPA -- this module is that baseline);
+  * a paged cache (the pages name paged attention but give no layout): a
+    pool [num_blocks, Hkv, block_size, D] and an integer block table
+    [B, max_blocks]; key row j of request b is row j % block_size of block
+    block_table[b, j // block_size].  With an appended token, kv_lens counts
+    it and its K/V go to row kv_lens[b] - 1 before attending.
 """
 
 from __future__ import annotations
@@ -155,3 +160,62 @@ def attention_q4(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias,
     k = dequant_q4(k_codes, k_scale, k_bias, group_size)
     v = dequant_q4(v_codes, v_scale, v_bias, group_size)
     return attention(q, k, v, kv_lens=kv_lens, scale=scale, causal=causal)
+
+
+def paged_to_contiguous(pool, block_table, kv_lens, block_size: int) -> np.ndarray:
+    """Gather a paged cache into a dense [B, Hkv, max(kv_lens), D] array.
+
+    pool: [num_blocks, Hkv, block_size, D]; block_table: [B, max_blocks].
+    Row j < kv_lens[b] of request b is pool[block_table[b, j // block_size],
+    :, j % block_size]; rows past kv_lens[b] are zero (never read).
+    """
+    pool = _f64(pool)
+    table = np.asarray(block_table, dtype=np.int64)
+    B = table.shape[0]
+    hkv, D = pool.shape[1], pool.shape[3]
+    S = max(1, int(max(kv_lens)))
+    out = np.zeros((B, hkv, S, D), dtype=np.float64)
+    for b in range(B):
+        for j in range(int(kv_lens[b])):
+            out[b, :, j, :] = pool[table[b, j // block_size], :, j % block_size, :]
+    return out
+
+
+def append_paged(k_pool, v_pool, block_table, kv_lens, block_size: int, k_new, v_new):
+    """Copies of the pools with the new token of every request written.
+
+    k_new, v_new: [B, Hkv, 1, D]; the token of request b goes to position
+    kv_lens[b] - 1, i.e. row (kv_lens[b] - 1) % block_size of block
+    block_table[b, (kv_lens[b] - 1) // block_size].  Requests with
+    kv_lens[b] == 0 write nothing.
+    """
+    kp = _f64(k_pool).copy()
+    vp = _f64(v_pool).copy()
+    table = np.asarray(block_table, dtype=np.int64)
+    kn, vn = _f64(k_new), _f64(v_new)
+    for b in range(table.shape[0]):
+        pos = int(kv_lens[b]) - 1
+        if pos < 0:
+            continue
+        blk = table[b, pos // block_size]
+        kp[blk, :, pos % block_size, :] = kn[b, :, 0, :]
+        vp[blk, :, pos % block_size, :] = vn[b, :, 0, :]
+    return kp, vp
+
+
+def attention_paged(q, k_pool, v_pool, block_table, kv_lens, block_size: int, scale=None,
+                    k_new=None, v_new=None):
+    """Decode attention over a paged cache: (append,) gather, then attend.
+
+    Returns the dict of ``attention`` plus ``k_pool`` and ``v_pool`` (the
+    pools after the append; the inputs are not modified).
+    """
+    kp, vp = _f64(k_pool), _f64(v_pool)
+    if k_new is not None:
+        kp, vp = append_paged(kp, vp, block_table, kv_lens, block_size, k_new, v_new)
+    k = paged_to_contiguous(kp, block_table, kv_lens, block_size)
+    v = paged_to_contiguous(vp, block_table, kv_lens, block_size)
+    out = attention(q, k, v, kv_lens=kv_lens, scale=scale)
+    out["k_pool"] = kp
+    out["v_pool"] = vp
+    return out

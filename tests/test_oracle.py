@@ -299,3 +299,104 @@ def test_pins_catch_swapped_nibbles(monkeypatch):
     x = oracle.dequant_q4(swapped, np.array(case["scale"], dtype=np.float16),
                           np.array(case["bias"], dtype=np.float16), group_size=case["group_size"])
     assert not np.array_equal(x, np.array(case["x"]))
+
+
+# --- paged cache: a relabeling of rows, and the append -------------------------
+
+@pytest.mark.parametrize("case", _cases()["paged_cases"], ids=lambda c: c["name"])
+def test_hand_paged_cases(case):
+    kn = np.array(case["k_new"]) if "k_new" in case else None
+    vn = np.array(case["v_new"]) if "v_new" in case else None
+    out = oracle.attention_paged(np.array(case["q"]), np.array(case["k_pool"]), np.array(case["v_pool"]),
+                                 case["block_table"], case["kv_lens"], case["block_size"],
+                                 scale=case["scale"], k_new=kn, v_new=vn)
+    np.testing.assert_allclose(out["o"], np.array(case["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["lse"], np.array(case["lse"]), rtol=0, atol=1e-12)
+    if "k_pool_after" in case:
+        np.testing.assert_array_equal(out["k_pool"], np.array(case["k_pool_after"]))
+        np.testing.assert_array_equal(out["v_pool"], np.array(case["v_pool_after"]))
+
+
+def _paged_from_contiguous(k, v, kv_lens, block_size, seed):
+    """Cut a contiguous cache into blocks, shuffle them into a larger pool
+    (with unused blocks full of NaN) and build the block table."""
+    B, hkv, S, D = k.shape
+    nb = -(-S // block_size)
+    n_pool = B * nb + 3
+    rng = np.random.default_rng(seed)
+    slots = rng.permutation(n_pool)
+    kp = np.full((n_pool, hkv, block_size, D), np.nan)
+    vp = np.full((n_pool, hkv, block_size, D), np.nan)
+    table = np.zeros((B, nb), dtype=np.int32)
+    for b in range(B):
+        for i in range(nb):
+            blk = slots[b * nb + i]
+            table[b, i] = blk
+            rows = slice(i * block_size, min(S, (i + 1) * block_size))
+            n = rows.stop - rows.start
+            kp[blk, :, :n] = k[b, :, rows]
+            vp[blk, :, :n] = v[b, :, rows]
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("block_size", [1, 4, 16])
+def test_paged_attention_equals_contiguous(block_size):
+    B, Hq, Hkv, S, D = 3, 6, 2, 37, 8
+    q = _rand((B, Hq, 1, D), 41)
+    k = _rand((B, Hkv, S, D), 42)
+    v = _rand((B, Hkv, S, D), 43)
+    kv_lens = [37, 1, 20]
+    kp, vp, table = _paged_from_contiguous(k, v, kv_lens, block_size, 44)
+    got = oracle.attention_paged(q, kp, vp, table, kv_lens, block_size)
+    want = oracle.attention(q, k, v, kv_lens=kv_lens)
+    np.testing.assert_allclose(got["o"], want["o"], rtol=0, atol=1e-12)
+    dense = oracle.paged_to_contiguous(kp, table, kv_lens, block_size)
+    for b, L in enumerate(kv_lens):
+        np.testing.assert_array_equal(dense[b, :, :L], k[b, :, :L])
+
+
+def test_paged_append_equals_contiguous_with_new_row():
+    B, Hq, Hkv, S, D, bs = 2, 4, 2, 24, 8, 8
+    q = _rand((B, Hq, 1, D), 51)
+    k = _rand((B, Hkv, S, D), 52)
+    v = _rand((B, Hkv, S, D), 53)
+    kn = _rand((B, Hkv, 1, D), 54)
+    vn = _rand((B, Hkv, 1, D), 55)
+    kv_lens = [17, 8]  # the new tokens land in row 0 of a block and in the last row of one
+    kp, vp, table = _paged_from_contiguous(k, v, kv_lens, bs, 56)
+    got = oracle.attention_paged(q, kp, vp, table, kv_lens, bs, k_new=kn, v_new=vn)
+    k2, v2 = k.copy(), v.copy()
+    for b, L in enumerate(kv_lens):
+        k2[b, :, L - 1] = kn[b, :, 0]
+        v2[b, :, L - 1] = vn[b, :, 0]
+    want = oracle.attention(q, k2, v2, kv_lens=kv_lens)
+    np.testing.assert_allclose(got["o"], want["o"], rtol=0, atol=1e-12)
+    # exactly the two slots changed in each pool
+    changed = ~np.isclose(got["k_pool"], kp, equal_nan=True)
+    assert changed.any(axis=(1, 3)).sum() == len(kv_lens)
+
+
+def test_pins_catch_paged_row_index_slip(monkeypatch):
+    def bad_gather(pool, block_table, kv_lens, block_size):
+        pool = np.asarray(pool, dtype=np.float64)
+        table = np.asarray(block_table, dtype=np.int64)
+        out = np.zeros((table.shape[0], pool.shape[1], max(1, int(max(kv_lens))), pool.shape[3]))
+        for b in range(table.shape[0]):
+            for j in range(int(kv_lens[b])):  # block index and row swapped
+                out[b, :, j, :] = pool[table[b, j % block_size], :, j // block_size, :]
+        return out
+    monkeypatch.setattr(gqa_oracle, "paged_to_contiguous", bad_gather)
+    # (the hand cases select the same set of rows either way: only a larger
+    # relabeling tells the two apart)
+    with pytest.raises((AssertionError, IndexError)):
+        test_paged_attention_equals_contiguous(4)
+
+
+def test_pins_catch_append_off_by_one(monkeypatch):
+    real = gqa_oracle.append_paged
+
+    def late_append(k_pool, v_pool, block_table, kv_lens, block_size, k_new, v_new):
+        return real(k_pool, v_pool, block_table, [int(x) + 1 for x in kv_lens], block_size, k_new, v_new)
+    monkeypatch.setattr(gqa_oracle, "append_paged", late_append)
+    with pytest.raises((AssertionError, IndexError)):
+        test_paged_append_equals_contiguous_with_new_row()
