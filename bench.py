@@ -267,6 +267,62 @@ def ragged_point(binding, B, device, stream, flush, iters=10):
     return {"B": B, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
 
 
+def paged_point(binding, B, device, stream, flush, iters=10, block_size=64):
+    """The ragged workload above on a paged cache (block size 64, blocks in a
+    random order in the pool) with the new token of every request appended
+    inside the call: Hq=32, Hkv=8, D=128, bf16, 36 layers."""
+    kv_lens = inputs.ragged_kv_lens(B, 64, 8192, seed=inputs.BASE_SEED + B)
+    lens_t = torch.from_numpy(kv_lens).to(device)
+    n_layers, hkv, D = 36, 8, 128
+    nbs = [-(-int(L) // block_size) for L in kv_lens]
+    max_blocks = 8192 // block_size  # the table spans max_kv_len; entries past a request's blocks are unused
+    layers = []
+    for l in range(n_layers):
+        n_pool = sum(nbs) + 4
+        kp = inputs.randn((n_pool, hkv, block_size, D), inputs.tensor_seed(l, 1), torch.bfloat16, device)
+        vp = inputs.randn((n_pool, hkv, block_size, D), inputs.tensor_seed(l, 2), torch.bfloat16, device)
+        perm = torch.from_numpy(np.random.default_rng(l).permutation(n_pool).astype(np.int32))
+        table = torch.zeros((B, max_blocks), dtype=torch.int32)
+        at = 0
+        for b, nb in enumerate(nbs):
+            table[b, :nb] = perm[at:at + nb]
+            at += nb
+        q = inputs.randn((B, 32, 1, D), inputs.tensor_seed(l, 0), torch.bfloat16, device)
+        kn = inputs.randn((B, hkv, 1, D), inputs.tensor_seed(l, 3), torch.bfloat16, device)
+        vn = inputs.randn((B, hkv, 1, D), inputs.tensor_seed(l, 4), torch.bfloat16, device)
+        layers.append((q, kp, vp, table.to(device), kn, vn))
+    outs = [torch.empty_like(x[0]) for x in layers]
+    ws = binding.decode_workspace(B, 32, hkv, D, 8192, binding.GQA_BF16, device)
+    torch.cuda.synchronize()
+
+    def step():
+        for (q, kp, vp, table, kn, vn), o in zip(layers, outs):
+            binding.gqa_attn_decode_paged(q, kn, vn, kp, vp, table, lens_t, o, D ** -0.5, ws, 8192,
+                                          stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    ts = []
+    for _ in range(iters):
+        with torch.cuda.stream(stream):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n_layers)
+    us = statistics.median(ts)
+    # Q, K, V of the valid rows and O, plus the appended token (read, then
+    # written into the pools)
+    nbytes = metrics.decode_bytes(32, hkv, D, kv_lens, 2) + 4 * B * hkv * D * 2
+    del layers, outs
+    torch.cuda.empty_cache()
+    return {"B": B, "block_size": block_size, "us_per_call": round(us, 3),
+            "GBps": round(nbytes / us / 1e3, 1)}
+
+
 def q4_point(binding, S, device, stream, flush, iters=10):
     """Hq=32, Hkv=8, D=128, B=4, 4-bit group-affine cache, 36 layer calls."""
     B, n_layers = 4, 36
@@ -436,6 +492,28 @@ def _case_inputs(name, device):
         nbytes = metrics.decode_bytes(32, 8, 128, lens, 2)
         return (lambda st: binding_mod().gqa_attn_decode(q, k, v, o, lens_t, 128 ** -0.5, ws, max_kv_len=8192,
                                                          stream=st)), nbytes, "bytes"
+    if name == "decode-bf16-paged-B64":
+        lens = inputs.ragged_kv_lens(64, 64, 8192, seed=inputs.BASE_SEED + 64)
+        lens_t = torch.from_numpy(lens).to(device)
+        nbs = [-(-int(L) // 64) for L in lens]
+        n_pool = sum(nbs)
+        kp = inputs.randn((n_pool, 8, 64, 128), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+        vp = inputs.randn((n_pool, 8, 64, 128), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+        perm = torch.from_numpy(np.random.default_rng(0).permutation(n_pool).astype(np.int32))
+        table = torch.zeros((64, 8192 // 64), dtype=torch.int32)
+        at = 0
+        for b, nb in enumerate(nbs):
+            table[b, :nb] = perm[at:at + nb]
+            at += nb
+        table = table.to(device)
+        q = inputs.randn((64, 32, 1, 128), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+        kn = inputs.randn((64, 8, 1, 128), inputs.tensor_seed(0, 3), torch.bfloat16, device)
+        vn = inputs.randn((64, 8, 1, 128), inputs.tensor_seed(0, 4), torch.bfloat16, device)
+        o = torch.empty_like(q)
+        ws = binding_mod().decode_workspace(64, 32, 8, 128, 8192, binding_mod().GQA_BF16, device)
+        nbytes = metrics.decode_bytes(32, 8, 128, lens, 2) + 4 * 64 * 8 * 128 * 2
+        return (lambda st: binding_mod().gqa_attn_decode_paged(q, kn, vn, kp, vp, table, lens_t, o, 128 ** -0.5,
+                                                               ws, 8192, stream=st)), nbytes, "bytes"
     if name == "q4-B4-S16384":
         S = 16384
         cache = inputs.q4_cache(4, 8, 128, S, device=device)
@@ -460,7 +538,8 @@ def _case_inputs(name, device):
     raise SystemExit(f"unknown kernel case {name!r}")
 
 
-KERNEL_CASES = ("decode-f32-S32768", "decode-bf16-S32768", "decode-bf16-ragged-B64", "q4-B4-S16384",
+KERNEL_CASES = ("decode-f32-S32768", "decode-bf16-S32768", "decode-bf16-ragged-B64", "decode-bf16-paged-B64",
+                "q4-B4-S16384",
                 "prefill-T4097", "prefill-T16384", "prefill-q512-kv4096")
 
 
@@ -665,6 +744,8 @@ def main():
                                                    for B in (1, 2, 4, 8, 16, 64)]
         line["q4_decode_qwen3_4b_B4_36_layers"] = [q4_point(binding, S, device, stream, flush)
                                                   for S in (64, 2048, 16384)]
+        line["paged_decode_qwen3_4b_36_layers"] = [paged_point(binding, B, device, stream, flush)
+                                                   for B in (16, 64)]
         pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
         pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
         line["prefill_causal_qwen05b_bf16"] = pf

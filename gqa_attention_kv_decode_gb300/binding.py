@@ -32,11 +32,13 @@ GQA_BF16 = 1
 GQA_DEV_KVLEN_CLAMPED = 1
 GQA_DEV_EMPTY_REQUEST = 2
 GQA_DEV_WAIT_TIMEOUT = 4
+GQA_DEV_BAD_BLOCK = 8
 
 EXPORTED = (
     "gqa_attn_decode_workspace_size",
     "gqa_attn_decode",
     "gqa_attn_decode_noalloc",
+    "gqa_attn_decode_paged",
     "gqa_attn_decode_q4_workspace_size",
     "gqa_attn_decode_q4",
     "gqa_attn_prefill",
@@ -74,6 +76,9 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode.restype = i32
     L.gqa_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
     L.gqa_attn_decode_noalloc.restype = i32
+    L.gqa_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, f32, i32, vp, sz, vp]
+    L.gqa_attn_decode_paged.restype = i32
     L.gqa_attn_decode_q4_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.gqa_attn_decode_q4_workspace_size.restype = sz
     L.gqa_attn_decode_q4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -164,6 +169,25 @@ def gqa_attn_decode_noalloc(q, k, v, o, kv_lens, scale, max_kv_len=None, stream=
     _check(rc, "gqa_attn_decode_noalloc")
 
 
+def gqa_attn_decode_paged(q, k_new, v_new, k_pool, v_pool, block_table, kv_lens, o, scale, workspace,
+                          max_kv_len, stream=None):
+    """q, o [B,Hq,1,D]; k_pool, v_pool [num_blocks,Hkv,block_size,D] (modified
+    when k_new, v_new [B,Hkv,1,D] are given: the new token goes to row
+    kv_lens[b]-1); block_table int32 [B,max_blocks]; kv_lens int32 [B]."""
+    B, Hq, Tq, D = q.shape
+    num_blocks, Hkv, block_size = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    if Tq != 1:
+        raise ValueError("decode takes one query row per request")
+    if block_table.dtype != torch.int32 or kv_lens.dtype != torch.int32:
+        raise TypeError("block_table and kv_lens are int32")
+    rc = lib().gqa_attn_decode_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                     _ptr(block_table), _ptr(kv_lens), _ptr(o), B, Hq, Hkv, D,
+                                     block_size, num_blocks, block_table.shape[1], int(max_kv_len),
+                                     float(scale), _dtype_code(q), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gqa_attn_decode_paged")
+
+
 def gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len) -> int:
     return lib().gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len)
 
@@ -241,6 +265,20 @@ def decode(q, k, v, kv_lens=None, scale=None, max_kv_len=None, workspace=None, s
         workspace = decode_workspace(B, Hq, Hkv, D, max_kv_len, _dtype_code(q), q.device)
     o = torch.empty_like(q)
     gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len, stream)
+    return o
+
+
+def decode_paged(q, k_pool, v_pool, block_table, kv_lens, max_kv_len, k_new=None, v_new=None,
+                 scale=None, workspace=None, stream=None):
+    B, Hq, _, D = q.shape
+    Hkv = k_pool.shape[1]
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, D, max_kv_len, _dtype_code(q), q.device)
+    o = torch.empty_like(q)
+    gqa_attn_decode_paged(q, k_new, v_new, k_pool, v_pool, block_table, kv_lens, o, scale, workspace,
+                          max_kv_len, stream)
     return o
 
 

@@ -186,6 +186,66 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
   return GQA_OK;
 }
 
+GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const void* v_new,
+                                       void* k_pool, void* v_pool, const int32_t* block_table,
+                                       const int32_t* kv_lens, void* o, int B, int Hq, int Hkv,
+                                       int D, int block_size, int num_blocks, int max_blocks,
+                                       int max_kv_len, float scale, int dtype, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  if (block_size < 1 || num_blocks < 1 || max_blocks < 1) return GQA_ERR_INVALID_ARG;
+  if (long(max_kv_len) > long(max_blocks) * block_size) return GQA_ERR_INVALID_ARG;
+  int rc = check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, scale);
+  if (rc != GQA_OK) return rc;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (block_size % decode_tile_rows(dtype, D) != 0) return GQA_ERR_UNSUPPORTED;
+  // block ids index [num_blocks * Hkv] (block, head) slabs of block_size rows
+  if (long(num_blocks) * Hkv > 0x7fffffffL || long(num_blocks) * Hkv * block_size > 0x7fffffffL)
+    return GQA_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  rc = check_ptrs({q, k_pool, v_pool, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  rc = check_ptrs({block_table, kv_lens}, dev, 4);
+  if (rc != GQA_OK) return rc;
+  if (k_new != nullptr) {
+    rc = check_ptrs({k_new, v_new}, dev, 16);
+    if (rc != GQA_OK) return rc;
+  }
+  if (workspace == nullptr) return GQA_ERR_WORKSPACE;
+  rc = check_ptrs({workspace}, dev, 256);
+  if (rc == GQA_ERR_INVALID_ARG) return GQA_ERR_WORKSPACE;
+  if (rc != GQA_OK) return rc;
+
+  DecodeArgs a;
+  a.q = q;
+  a.k = k_pool;
+  a.v = v_pool;
+  a.o = o;
+  a.kv_lens = kv_lens;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S_cap = block_size;
+  a.max_kv_len = max_kv_len;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.workspace = workspace;
+  a.block_table = block_table;
+  a.block_size = block_size;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
+                       decode_ctas_per_sm(dtype));
+  if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
+    return GQA_ERR_WORKSPACE;
+  if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
 GQA_ATTN_API size_t gqa_attn_decode_q4_workspace_size(int B, int Hq, int Hkv, int D,
                                                       int max_kv_len) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;

@@ -52,6 +52,11 @@ struct DecodeParams {
   float2* ml;     // [B][Hq][n_split] (max in log2 units, sum)
   float* part_o;  // [B][Hq][n_split][D] unnormalised partial outputs
   uint64_t wait_limit_ns;
+  // paged cache (PAGED kernels): k and v are pools [num_blocks][Hkv][block_size][D]
+  const int32_t* block_table;  // [B][max_blocks]
+  int block_size, max_blocks, num_blocks;
+  const void* k_new;  // [B][Hkv][D]: token appended at row kv_lens[b] - 1, or null
+  const void* v_new;
 };
 
 
@@ -93,7 +98,11 @@ struct Cfg {
   static_assert(NREP >= 1 && NREP <= 8, "at most 8 query heads per CTA");
 };
 
-template <typename T, int D, int NREP, int R_, int NSTAGE>
+// PAGED: K and V are block pools addressed through the block table; a tile
+// (a multiple of which the block size is) never crosses a block.  With k_new
+// the CTA that owns row kv_len - 1 writes the new token into its tile in
+// shared memory and into the pool.
+template <typename T, int D, int NREP, int R_, int NSTAGE, bool PAGED>
 __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
     decode_split_kernel(const DecodeParams p) {
   using C = Cfg<T, D, NREP, R_, NSTAGE>;
@@ -108,7 +117,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   const int b = blockIdx.z;
   const int h0 = g * p.n_rep + hc * p.nrep_cta;
   const int nh = min(p.nrep_cta, p.n_rep - hc * p.nrep_cta);
-  const size_t head_row0 = (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
+  const size_t head_row0 = PAGED ? 0 : (size_t(b) * p.Hkv + g) * size_t(p.S_cap);
   const unsigned char* kbase = static_cast<const unsigned char*>(p.k) + head_row0 * C::ROWB;
   const unsigned char* vbase = static_cast<const unsigned char*>(p.v) + head_row0 * C::ROWB;
 
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   // grid_dependency_wait() returns nothing may be read or written; the first
   // tiles this split will copy (assuming kv_len = max_kv_len, which only the
   // ragged case can make wrong) are meanwhile prefetched into L2.
-  if (tid == 0 && hc == 0) {
+  if (!PAGED && tid == 0 && hc == 0) {  // (a paged cache's rows are known only after the wait)
     for (int t = 0; t < NSTAGE; ++t) {
       const int row0 = (split + t * p.n_split) * TILE;
       if (row0 >= p.max_kv_len) break;
@@ -156,15 +165,35 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   int* rel = reinterpret_cast<int*>(smem + C::OFF_BAR + NSTAGE * 8);  // warps done with a stage
   volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [2] issued
 
+  // Byte offset of key row `row` of this (request, KV head) in K or V.  For a
+  // paged cache the block id comes from the table; an id outside the pool is
+  // reported and replaced by block 0, so no copy ever leaves the pool.
+  auto row_offset = [&](int row) -> size_t {
+    if constexpr (PAGED) {
+      int blk = p.block_table[size_t(b) * p.max_blocks + row / p.block_size];
+      if (blk < 0 || blk >= p.num_blocks) {
+        atomicOr(p.status, GQA_DEV_BAD_BLOCK);
+        blk = 0;
+      }
+      return ((size_t(blk) * p.Hkv + g) * p.block_size + row % p.block_size) * C::ROWB;
+    } else {
+      return size_t(row) * C::ROWB;
+    }
+  };
   // Copy k-th tile of this split into stage st (one elected thread).
   auto issue = [&](int kt, int st, uint64_t pol) {
     const int row0 = (split + kt * n_used) * TILE;
     const uint32_t bytes = uint32_t(min(TILE, L - row0)) * C::ROWB;
     unsigned char* dst = smem + st * C::STAGEB;
+    const size_t off = row_offset(row0);
     mbar_arrive_expect_tx(&full[st], 2 * bytes);
-    bulk_g2s(dst, kbase + size_t(row0) * C::ROWB, bytes, &full[st], pol);
-    bulk_g2s(dst + C::TILEB, vbase + size_t(row0) * C::ROWB, bytes, &full[st], pol);
+    bulk_g2s(dst, kbase + off, bytes, &full[st], pol);
+    bulk_g2s(dst + C::TILEB, vbase + off, bytes, &full[st], pol);
   };
+  // The appended token (row L - 1) lies in tile (L - 1) / TILE, which is
+  // tile t_new of split ((L - 1) / TILE) % n_used.
+  int t_new = -1;
+  if (PAGED && p.k_new != nullptr && ((L - 1) / TILE) % n_used == split) t_new = ((L - 1) / TILE) / n_used;
   if (tid == 0) {  // barriers, then the first NSTAGE copies before q is staged
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1);
@@ -241,6 +270,23 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
       const int st = t % NSTAGE;
       const bool ok = wait_or_abort(&full[st], uint32_t(t / NSTAGE) & 1u, flag, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (PAGED && t == t_new && warp == ((L - 1) % TILE) / C::TW) {
+        // the warp that reads row L - 1 puts the new token there (over the
+        // stale cache row just copied) and into the pool
+        const int r = (L - 1) % TILE;
+        if (lane < C::NCH) {
+          const size_t src = (size_t(b) * p.Hkv + g) * C::ROWB + lane * 16;
+          const uint4 kx = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.k_new) + src);
+          const uint4 vx = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.v_new) + src);
+          *reinterpret_cast<uint4*>(smem + st * C::STAGEB + r * C::ROWB + lane * 16) = kx;
+          *reinterpret_cast<uint4*>(smem + st * C::STAGEB + C::TILEB + r * C::ROWB + lane * 16) = vx;
+          const size_t off = row_offset(L - 1) + lane * 16;
+          *reinterpret_cast<uint4*>(const_cast<unsigned char*>(kbase) + off) = kx;
+          *reinterpret_cast<uint4*>(const_cast<unsigned char*>(vbase) + off) = vx;
+        }
+        fence_proxy_async_smem();  // before the stage can be refilled by a copy
+        __syncwarp();
+      }
       const int nvalid = min(TILE, L - (split + t * n_used) * TILE);
       const int wrow0 = warp * C::TW;
       const int wvalid = min(C::TW, nvalid - wrow0);
@@ -471,10 +517,10 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   }
 }
 
-template <typename T, int D, int NREP, int R, int NSTAGE>
+template <typename T, int D, int NREP, int R, int NSTAGE, bool PAGED>
 cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   using C = Cfg<T, D, NREP, R, NSTAGE>;
-  auto kern = decode_split_kernel<T, D, NREP, R, NSTAGE>;
+  auto kern = decode_split_kernel<T, D, NREP, R, NSTAGE, PAGED>;
   static bool configured = false;  // per instantiation; attribute is per-function
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -498,19 +544,19 @@ struct TileCfg;
 template <> struct TileCfg<float, 128> { static constexpr int R = 2, NSTAGE = 3, TILE = 64; };
 template <> struct TileCfg<float, 64> { static constexpr int R = 4, NSTAGE = 3, TILE = 128; };
 
-template <typename T, int D>
+template <typename T, int D, bool PAGED>
 cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
   constexpr int TL = TileCfg<T, D>::R, NS = TileCfg<T, D>::NSTAGE;
   static_assert(Cfg<T, D, 8, TL, NS>::TILE == TileCfg<T, D>::TILE, "tile height");
   switch (p.nrep_cta) {
-    case 1: return launch_one<T, D, 1, TL, NS>(p, grid, s);
-    case 2: return launch_one<T, D, 2, TL, NS>(p, grid, s);
+    case 1: return launch_one<T, D, 1, TL, NS, PAGED>(p, grid, s);
+    case 2: return launch_one<T, D, 2, TL, NS, PAGED>(p, grid, s);
     case 3:
-    case 4: return launch_one<T, D, 4, TL, NS>(p, grid, s);
+    case 4: return launch_one<T, D, 4, TL, NS, PAGED>(p, grid, s);
     case 5:
     case 6:
-    case 7: return launch_one<T, D, 7, TL, NS>(p, grid, s);
-    default: return launch_one<T, D, 8, TL, NS>(p, grid, s);
+    case 7: return launch_one<T, D, 7, TL, NS, PAGED>(p, grid, s);
+    default: return launch_one<T, D, 8, TL, NS, PAGED>(p, grid, s);
   }
 }
 
@@ -549,10 +595,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
+  p.block_table = a.block_table;
+  p.block_size = a.block_size;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.k_new = a.k_new;
+  p.v_new = a.v_new;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
-  const cudaError_t e = a.dtype == GQA_F32 ? (a.D == 128 ? dispatch_nrep<float, 128>(p, grid, stream)
-                                                          : dispatch_nrep<float, 64>(p, grid, stream))
-                                           : launch_decode_mma(a, stream);
+  cudaError_t e;
+  if (a.dtype != GQA_F32)
+    e = launch_decode_mma(a, stream);
+  else if (a.block_table != nullptr)
+    e = a.D == 128 ? dispatch_nrep<float, 128, true>(p, grid, stream) : dispatch_nrep<float, 64, true>(p, grid, stream);
+  else
+    e = a.D == 128 ? dispatch_nrep<float, 128, false>(p, grid, stream) : dispatch_nrep<float, 64, false>(p, grid, stream);
   if (e != cudaSuccess || a.plan.n_split == 1) return e;
   MergeParams m;
   m.o = p.o;

@@ -48,6 +48,14 @@ struct MmaParams {
   float2* ml;
   float* part_o;
   uint64_t wait_limit_ns;
+  // paged cache (PAGED kernels): the tensor maps span the pools
+  // [num_blocks * Hkv][block_size][D]
+  const int32_t* block_table;  // [B][max_blocks]
+  int block_size, max_blocks, num_blocks;
+  const __nv_bfloat16* k_new;  // [B][Hkv][D]: token appended at row kv_lens[b] - 1, or null
+  const __nv_bfloat16* v_new;
+  unsigned char* k_pool;       // pool bases, written by the append
+  unsigned char* v_pool;
 };
 
 template <int D, int NSTAGE>
@@ -101,7 +109,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int D, int NSTAGE>
+// PAGED: K and V tiles come from block pools through the block table (a tile
+// never crosses a block); with k_new the CTA that owns row kv_len - 1 writes
+// the new token into its tile in shared memory and into the pool.
+template <int D, int NSTAGE, bool PAGED>
 __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const MmaParams p) {
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
   if (tid == 0 && hc == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    for (int t = 0; t < NSTAGE; ++t) {
+    for (int t = 0; t < (PAGED ? 0 : NSTAGE); ++t) {  // (a paged cache's rows are known only after the wait)
       const int row0 = (split + t * p.n_split) * TILE;
       if (row0 >= p.max_kv_len) break;
       const uint32_t bytes = uint32_t(min(TILE, p.max_kv_len - row0)) * D * 2;
@@ -163,17 +174,40 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
   // k-th tile of this split into stage st: K then V, each HALVES boxes of
   // 64 keys x 64 dims.  Rows past S_cap arrive as zeros; rows in [L, S_cap)
   // arrive as whatever the cache holds there (masked below).
+  // (row within the map, map head) of key row `row`.  For a paged cache the
+  // block id comes from the table; an id outside the pool is reported and
+  // replaced by block 0.
+  auto map_coord = [&](int row, int& mrow, int& mhead) {
+    if constexpr (PAGED) {
+      int blk = p.block_table[size_t(b) * p.max_blocks + row / p.block_size];
+      if (blk < 0 || blk >= p.num_blocks) {
+        atomicOr(p.status, GQA_DEV_BAD_BLOCK);
+        blk = 0;
+      }
+      mrow = row % p.block_size;
+      mhead = blk * p.Hkv + g;
+    } else {
+      mrow = row;
+      mhead = kv_head;
+    }
+  };
   auto issue = [&](int kt, int st) {
     const int row0 = (split + kt * n_used) * TILE;
+    int mrow, mhead;
+    map_coord(row0, mrow, mhead);
     unsigned char* dst = smem + st * C::STAGEB;
     mbar_arrive_expect_tx(&full[st], C::STAGEB);
 #pragma unroll
     for (int hf = 0; hf < C::HALVES; ++hf)
-      tma_load_3d(dst + hf * C::BOX, &tmK, hf * 64, row0, kv_head, &full[st]);
+      tma_load_3d(dst + hf * C::BOX, &tmK, hf * 64, mrow, mhead, &full[st]);
 #pragma unroll
     for (int hf = 0; hf < C::HALVES; ++hf)
-      tma_load_3d(dst + C::TILEB + hf * C::BOX, &tmV, hf * 64, row0, kv_head, &full[st]);
+      tma_load_3d(dst + C::TILEB + hf * C::BOX, &tmV, hf * 64, mrow, mhead, &full[st]);
   };
+  // The appended token (row L - 1) lies in tile (L - 1) / TILE, which is
+  // tile t_new of split ((L - 1) / TILE) % n_used.
+  int t_new = -1;
+  if (PAGED && p.k_new != nullptr && ((L - 1) / TILE) % n_used == split) t_new = ((L - 1) / TILE) / n_used;
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1);
@@ -213,6 +247,27 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
     const int row0 = (split + t * n_used) * TILE;
     const int wvalid = min(TILE, L - row0) - kb;  // valid keys among this warp's 16
     const uint32_t kaddr = sbase + st * C::STAGEB, vaddr = kaddr + C::TILEB;
+    if (PAGED && t == t_new && warp == ((L - 1) % TILE) / 16) {
+      // the warp that reads row L - 1 puts the new token there (over the
+      // stale cache row just copied; 128-byte swizzled layout) and into the pool
+      const int r = (L - 1) % TILE;
+      if (lane < C::HALVES * 8) {
+        const int hf = lane >> 3, ch = lane & 7;
+        const size_t src = (size_t(b) * p.Hkv + g) * D + hf * 64 + ch * 8;
+        const uint4 kx = *reinterpret_cast<const uint4*>(p.k_new + src);
+        const uint4 vx = *reinterpret_cast<const uint4*>(p.v_new + src);
+        unsigned char* kt = smem + st * C::STAGEB + hf * C::BOX + swz(r, ch);
+        *reinterpret_cast<uint4*>(kt) = kx;
+        *reinterpret_cast<uint4*>(kt + C::TILEB) = vx;
+        int mrow, mhead;
+        map_coord(L - 1, mrow, mhead);
+        const size_t dst = ((size_t(mhead) * p.block_size + mrow) * D + hf * 64 + ch * 8) * 2;
+        *reinterpret_cast<uint4*>(p.k_pool + dst) = kx;
+        *reinterpret_cast<uint4*>(p.v_pool + dst) = vx;
+      }
+      fence_proxy_async_smem();  // before the stage can be refilled by TMA
+      __syncwarp();
+    }
     if (wvalid > 0) {
       if (wvalid < 16) {
         // V rows past kv_len may hold anything (NaN included): 0 x NaN would
@@ -377,11 +432,11 @@ bool kv_map(CUtensorMap* out, const void* base, int D, int S_cap, int heads) {
   return true;
 }
 
-template <int D, int NSTAGE>
+template <int D, int NSTAGE, bool PAGED>
 cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& p, dim3 grid,
                        cudaStream_t stream) {
   using C = MmaCfg<D, NSTAGE>;
-  auto kern = decode_mma_kernel<D, NSTAGE>;
+  auto kern = decode_mma_kernel<D, NSTAGE, PAGED>;
   static std::once_flag once;
   static cudaError_t cfg_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -399,8 +454,10 @@ cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPa
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   if (a.D != 64 && a.D != 128) return cudaErrorNotSupported;
   CUtensorMap tk, tv;
-  const int heads = a.B * a.Hkv;
-  if (!kv_map(&tk, a.k, a.D, a.S_cap, heads) || !kv_map(&tv, a.v, a.D, a.S_cap, heads)) return cudaErrorInvalidValue;
+  const bool paged = a.block_table != nullptr;
+  const int heads = paged ? a.num_blocks * a.Hkv : a.B * a.Hkv;
+  const int rows = paged ? a.block_size : a.S_cap;
+  if (!kv_map(&tk, a.k, a.D, rows, heads) || !kv_map(&tv, a.v, a.D, rows, heads)) return cudaErrorInvalidValue;
   MmaParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -424,8 +481,18 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
+  p.block_table = a.block_table;
+  p.block_size = a.block_size;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  p.k_pool = static_cast<unsigned char*>(const_cast<void*>(a.k));
+  p.v_pool = static_cast<unsigned char*>(const_cast<void*>(a.v));
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
-  return a.D == 128 ? launch_mma<128, 3>(tk, tv, p, grid, stream) : launch_mma<64, 6>(tk, tv, p, grid, stream);
+  if (paged)
+    return a.D == 128 ? launch_mma<128, 3, true>(tk, tv, p, grid, stream) : launch_mma<64, 6, true>(tk, tv, p, grid, stream);
+  return a.D == 128 ? launch_mma<128, 3, false>(tk, tv, p, grid, stream) : launch_mma<64, 6, false>(tk, tv, p, grid, stream);
 }
 
 }  // namespace gqa

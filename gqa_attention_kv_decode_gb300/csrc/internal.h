@@ -56,6 +56,13 @@ struct DecodeArgs {
   int dtype;
   void* workspace;
   SplitPlan plan;
+  // paged cache (block_table != nullptr): k and v are pools
+  // [num_blocks][Hkv][block_size][D]; k_new / v_new (or null) is appended at
+  // row kv_lens[b] - 1 of each request before it attends
+  const int32_t* block_table = nullptr;
+  int block_size = 0, max_blocks = 0, num_blocks = 0;
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
 };
 
 // Tile height (rows) of the decode kernel for this dtype / head size, and how

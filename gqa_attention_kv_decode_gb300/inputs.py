@@ -95,3 +95,33 @@ def q4_cache(B, Hkv, D, s_cap, layer=0, device="cpu", group_size=64, base=BASE_S
     kc, ks, kb = quantize_q4(k, group_size)
     vc, vs, vb = quantize_q4(v, group_size)
     return kc, ks, kb, vc, vs, vb
+
+
+def paged_pool(k: torch.Tensor, v: torch.Tensor, kv_lens, block_size: int, seed: int, spare: int = 3,
+               fill=float("nan")):
+    """Scatter a dense cache [B, Hkv, S, D] into block pools.
+
+    Returns (k_pool, v_pool, block_table): pools [num_blocks, Hkv, block_size,
+    D] with the blocks of all requests in a seeded random order, ``spare``
+    extra blocks and every row past kv_lens[b] set to ``fill``; block_table
+    int32 [B, ceil(S / block_size)] (on the device of ``k``).  Key row j of
+    request b is row j % block_size of block block_table[b, j // block_size].
+    """
+    B, hkv, S, D = k.shape
+    nb = -(-S // block_size)
+    n_pool = B * nb + spare
+    order = np.random.default_rng(seed).permutation(n_pool)
+    kp = torch.full((n_pool, hkv, block_size, D), fill, dtype=k.dtype, device=k.device)
+    vp = torch.full_like(kp, fill)
+    table = torch.zeros((B, nb), dtype=torch.int32)
+    for b in range(B):
+        L = int(kv_lens[b])
+        for i in range(nb):
+            blk = int(order[b * nb + i])
+            table[b, i] = blk
+            r0 = i * block_size
+            n = max(0, min(block_size, L - r0))
+            if n:
+                kp[blk, :, :n] = k[b, :, r0:r0 + n]
+                vp[blk, :, :n] = v[b, :, r0:r0 + n]
+    return kp, vp, table.to(k.device)

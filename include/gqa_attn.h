@@ -75,6 +75,7 @@ typedef enum gqa_dtype {
 #define GQA_DEV_KVLEN_CLAMPED 1u /* some kv_lens[b] < 0 or > max_kv_len: clamped */
 #define GQA_DEV_EMPTY_REQUEST 2u /* some kv_lens[b] == 0: that output is zeros    */
 #define GQA_DEV_WAIT_TIMEOUT 4u  /* a bounded wait on a tile copy gave up          */
+#define GQA_DEV_BAD_BLOCK 8u     /* a paged-cache block id was outside the pool    */
 
 /* ---------------------------------------------------------------------------
  * Single-token decode (q_len = 1), split-KV with a log-sum-exp combine.
@@ -105,6 +106,48 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
                                  const int32_t* kv_lens, int B, int Hq, int Hkv, int D,
                                  int S_cap, int max_kv_len, float scale, int dtype,
                                  void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-token decode over a PAGED KV cache, with an optional fused append of
+ * the new token.
+ *
+ * The decode kernel reads only the head stride of K and V and needs the rows
+ * of a head next to each other; a cache kept in another layout had to be
+ * copied first ("Fused attention makes a 4,096-token Qwen2 prefill on Metal
+ * 4.5x faster", section "Cause and workaround", item 3).  Paged attention
+ * (named in "2x Faster Qwen2 Decode on Metal in Candle", section "Why It
+ * Matters", for the author's CPU engine) keeps the cache in fixed-size
+ * blocks instead; the pages give no layout, so this one is the library's:
+ *
+ *   q            [B, Hq, 1, D]                       dtype
+ *   k_pool,      [num_blocks, Hkv, block_size, D]    dtype; the rows of one
+ *   v_pool                                            (block, KV head) are contiguous
+ *   block_table  device int32 [B, max_blocks]: key row j of request b is row
+ *                j % block_size of block block_table[b][j / block_size].
+ *                Entries past the request's last block are never read.  An
+ *                id outside [0, num_blocks) sets GQA_DEV_BAD_BLOCK; that
+ *                request's output is then unspecified (no read leaves the pool).
+ *   kv_lens      device int32 [B] (required): keys per request, counting the
+ *                appended token; clamped like gqa_attn_decode's.
+ *   k_new, v_new [B, Hkv, 1, D] dtype, or both NULL.  When given, the token of
+ *                request b is written to key row kv_lens[b] - 1 (into the
+ *                pools, which the call therefore modifies) and attended to in
+ *                the same call.  Requests with kv_lens[b] == 0 write nothing.
+ *   o            [B, Hq, 1, D] dtype (written)
+ *   block_size   a positive multiple of the decode tile: 64 (bf16, or fp32
+ *                with D = 128) or 128 (fp32 with D = 64); else
+ *                GQA_ERR_UNSUPPORTED.
+ *   max_kv_len   host upper bound of kv_lens, <= max_blocks * block_size.
+ *   workspace    as for gqa_attn_decode (gqa_attn_decode_workspace_size with
+ *                the same B, Hq, Hkv, D, max_kv_len, dtype).
+ * Other arguments and errors as for gqa_attn_decode.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const void* v_new,
+                                       void* k_pool, void* v_pool, const int32_t* block_table,
+                                       const int32_t* kv_lens, void* o, int B, int Hq, int Hkv,
+                                       int D, int block_size, int num_blocks, int max_blocks,
+                                       int max_kv_len, float scale, int dtype, void* workspace,
+                                       size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Single-token decode without any caller-provided or allocated scratch.
