@@ -15,4 +15,5 @@ from .gqa_oracle import (  # noqa: F401
     paged_to_contiguous,
     append_paged,
     attention_paged,
+    quantize_q4,
 )

@@ -33,6 +33,11 @@ design notes):
     sections "The setup" and "Part 4: the other half of the lever actually
     works": the fused kernel reads the group-affine codes, the baseline
     dequantises them and calls SDPA -- this module is that baseline);
+  * the 4-bit quantizer (the pages say "group-affine", x = code*scale + bias,
+    and give no quantizer): per group, scale = fp16((max - min) / 15),
+    bias = fp16(min), code = clamp(round_half_even((x - bias) / scale), 0,
+    15), code 0 when scale == 0; computed in float32, the precision in which
+    the GPU kernel takes the same integer decisions;
   * a paged cache (the pages name paged attention but give no layout): a
     pool [num_blocks, Hkv, block_size, D] and an integer block table
     [B, max_blocks]; key row j of request b is row j % block_size of block
@@ -219,3 +224,33 @@ def attention_paged(q, k_pool, v_pool, block_table, kv_lens, block_size: int, sc
     out["k_pool"] = kp
     out["v_pool"] = vp
     return out
+
+
+def quantize_q4(x, group_size: int = 64):
+    """Group-affine 4-bit quantization of x [..., D] (float32 arithmetic).
+
+    Per group of ``group_size`` consecutive elements along D: the minimum and
+    maximum m, M; scale = fp16((M - m) / 15) and bias = fp16(m) (round to
+    nearest); code = round-half-even((x - bias) / scale) clamped to [0, 15],
+    and 0 where the scale is 0.  Codes are packed two per byte, element 2t in
+    the low nibble of byte t.  Returns (codes uint8 [..., D/2], scale fp16,
+    bias fp16 [..., D/group_size]).  ("Batching Decode Attention Across
+    Requests ...", VeloxQuant-MLX blog, "Part 4": the cache is quantized
+    incrementally, one newly aged group-aligned block per step.)
+    """
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    if D % group_size != 0 or D % 2 != 0:
+        raise ValueError("D must be a multiple of the group size")
+    grp = x.reshape(x.shape[:-1] + (D // group_size, group_size))
+    lo = grp.min(axis=-1)
+    hi = grp.max(axis=-1)
+    scale = ((hi - lo) / np.float32(15.0)).astype(np.float16)
+    bias = lo.astype(np.float16)
+    s32 = scale.astype(np.float32)[..., None]
+    b32 = bias.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint((grp - b32) / s32)
+    q = np.where(s32 > 0, np.clip(q, 0, 15), 0).astype(np.uint8).reshape(x.shape)
+    packed = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    return packed, scale, bias

@@ -400,3 +400,45 @@ def test_pins_catch_append_off_by_one(monkeypatch):
     monkeypatch.setattr(gqa_oracle, "append_paged", late_append)
     with pytest.raises((AssertionError, IndexError)):
         test_paged_append_equals_contiguous_with_new_row()
+
+
+# --- the 4-bit quantizer --------------------------------------------------------
+
+@pytest.mark.parametrize("case", _cases()["quantizer_cases"], ids=lambda c: c["name"])
+def test_hand_quantizer_cases(case):
+    c, s, b = oracle.quantize_q4(np.array(case["x"], dtype=np.float32), case["group_size"])
+    np.testing.assert_array_equal(c, np.array(case["codes"], dtype=np.uint8))
+    np.testing.assert_array_equal(s.astype(np.float64), np.array(case["scale"]))
+    np.testing.assert_array_equal(b.astype(np.float64), np.array(case["bias"]))
+
+
+def test_quantizer_invariants():
+    """Round trip within half a step; the group minimum gets code 0 and the
+    maximum code 15; codes are monotone in x within a group."""
+    x = torch.randn((3, 5, 256), generator=torch.Generator().manual_seed(61)).to(torch.bfloat16).float().numpy()
+    c, s, b = oracle.quantize_q4(x)
+    deq = oracle.dequant_q4(c, s, b)
+    step = np.repeat(s.astype(np.float64), 64, axis=-1)
+    assert (np.abs(deq - x) <= 0.5 * step + 1e-2 * step + 2e-3).all()
+    codes = np.empty(x.shape, dtype=np.int64)
+    codes[..., 0::2] = c & 15
+    codes[..., 1::2] = c >> 4
+    g = x.reshape(3, 5, 4, 64)
+    cg = codes.reshape(3, 5, 4, 64)
+    assert (np.take_along_axis(cg, g.argmin(-1)[..., None], -1) == 0).all()
+    assert (np.take_along_axis(cg, g.argmax(-1)[..., None], -1) == 15).all()
+    order = np.argsort(g, axis=-1, kind="stable")
+    assert (np.diff(np.take_along_axis(cg, order, -1), axis=-1) >= 0).all()
+
+
+def test_pins_catch_quantizer_slips(monkeypatch):
+    real = np.rint
+    monkeypatch.setattr(np, "rint", np.trunc)  # round toward zero instead of to nearest even
+    with pytest.raises(AssertionError):
+        for case in _cases()["quantizer_cases"]:
+            test_hand_quantizer_cases(case)
+    monkeypatch.setattr(np, "rint", real)
+    case = _cases()["quantizer_cases"][0]
+    c, _, _ = oracle.quantize_q4(np.array(case["x"], dtype=np.float32))
+    swapped = ((c & 15) << 4) | (c >> 4)
+    assert not np.array_equal(swapped, np.array(case["codes"], dtype=np.uint8))
