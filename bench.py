@@ -323,6 +323,49 @@ def paged_point(binding, B, device, stream, flush, iters=10, block_size=64):
             "GBps": round(nbytes / us / 1e3, 1)}
 
 
+def quantize_point(binding, device, stream, flush, iters=10):
+    """4-bit quantization of KV rows (Hkv=8, D=128, B=4): a whole 16384-token K
+    cache in one call (HBM-bound), and the per-step flush of one aged block of
+    64 tokens of K and of V (launch-bound) over 36 layers."""
+    B, hkv, D, S = 4, 8, 128, 16384
+    x = inputs.randn((B, hkv, S, D), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+    codes = torch.empty((B, hkv, S, D // 2), dtype=torch.uint8, device=device)
+    scale = torch.empty((B, hkv, S, D // 64), dtype=torch.float16, device=device)
+    bias = torch.empty_like(scale)
+    blocks = [inputs.randn((B, hkv, 64, D), inputs.tensor_seed(l, 5 + t), torch.bfloat16, device)
+              for l in range(36) for t in range(2)]
+    torch.cuda.synchronize()
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(iters):
+            with torch.cuda.stream(stream):
+                flush_l2(flush)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / n)
+        return statistics.median(ts)
+    full = lambda: binding.gqa_attn_quantize_q4(x, codes, scale, bias, stream=stream)
+    step = lambda: [binding.gqa_attn_quantize_q4(blk, codes, scale, bias, dst_row0=8192, stream=stream)
+                    for blk in blocks]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            full()
+            step()
+    us_full = timed(full, 1)
+    us_flush = timed(step, 36)
+    rows = B * hkv * S
+    nbytes = metrics.quantize_bytes(rows, D)
+    del x, codes, scale, bias, blocks
+    torch.cuda.empty_cache()
+    return {"full_cache_B4_S16384": {"us": round(us_full, 3), "GBps": round(nbytes / us_full / 1e3, 1)},
+            "flush_64_tokens_K_and_V": {"us_per_layer": round(us_flush, 3)}}
+
+
 def q4_point(binding, S, device, stream, flush, iters=10):
     """Hq=32, Hkv=8, D=128, B=4, 4-bit group-affine cache, 36 layer calls."""
     B, n_layers = 4, 36
@@ -514,6 +557,13 @@ def _case_inputs(name, device):
         nbytes = metrics.decode_bytes(32, 8, 128, lens, 2) + 4 * 64 * 8 * 128 * 2
         return (lambda st: binding_mod().gqa_attn_decode_paged(q, kn, vn, kp, vp, table, lens_t, o, 128 ** -0.5,
                                                                ws, 8192, stream=st)), nbytes, "bytes"
+    if name == "quantize-B4-S16384":
+        x = inputs.randn((4, 8, 16384, 128), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+        codes = torch.empty((4, 8, 16384, 64), dtype=torch.uint8, device=device)
+        scale = torch.empty((4, 8, 16384, 2), dtype=torch.float16, device=device)
+        bias = torch.empty_like(scale)
+        nbytes = metrics.quantize_bytes(4 * 8 * 16384, 128)
+        return (lambda st: binding_mod().gqa_attn_quantize_q4(x, codes, scale, bias, stream=st)), nbytes, "bytes"
     if name == "q4-B4-S16384":
         S = 16384
         cache = inputs.q4_cache(4, 8, 128, S, device=device)
@@ -539,7 +589,7 @@ def _case_inputs(name, device):
 
 
 KERNEL_CASES = ("decode-f32-S32768", "decode-bf16-S32768", "decode-bf16-ragged-B64", "decode-bf16-paged-B64",
-                "q4-B4-S16384",
+                "q4-B4-S16384", "quantize-B4-S16384",
                 "prefill-T4097", "prefill-T16384", "prefill-q512-kv4096")
 
 
@@ -746,6 +796,7 @@ def main():
                                                   for S in (64, 2048, 16384)]
         line["paged_decode_qwen3_4b_36_layers"] = [paged_point(binding, B, device, stream, flush)
                                                    for B in (16, 64)]
+        line["quantize_q4_qwen3_4b"] = quantize_point(binding, device, stream, flush)
         pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
         pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
         line["prefill_causal_qwen05b_bf16"] = pf

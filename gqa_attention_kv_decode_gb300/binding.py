@@ -39,6 +39,7 @@ EXPORTED = (
     "gqa_attn_decode",
     "gqa_attn_decode_noalloc",
     "gqa_attn_decode_paged",
+    "gqa_attn_quantize_q4",
     "gqa_attn_decode_q4_workspace_size",
     "gqa_attn_decode_q4",
     "gqa_attn_prefill",
@@ -79,6 +80,9 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                         i32, f32, i32, vp, sz, vp]
     L.gqa_attn_decode_paged.restype = i32
+    i64 = ctypes.c_int64
+    L.gqa_attn_quantize_q4.argtypes = [vp, i64, vp, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+    L.gqa_attn_quantize_q4.restype = i32
     L.gqa_attn_decode_q4_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.gqa_attn_decode_q4_workspace_size.restype = sz
     L.gqa_attn_decode_q4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -186,6 +190,20 @@ def gqa_attn_decode_paged(q, k_new, v_new, k_pool, v_pool, block_table, kv_lens,
                                      float(scale), _dtype_code(q), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "gqa_attn_decode_paged")
+
+
+def gqa_attn_quantize_q4(src, codes, scale, bias, dst_row0=0, rows=None, group_size=64, stream=None):
+    """src bf16 [B,Hkv,S_src,D]; codes uint8 [B,Hkv,S_cap,D/2]; scale, bias fp16
+    [B,Hkv,S_cap,D/64]: rows [0, rows) of src go to rows [dst_row0, dst_row0 + rows)."""
+    B, Hkv, S_src, D = src.shape
+    if src.dtype != torch.bfloat16 or codes.dtype != torch.uint8:
+        raise TypeError("bf16 source, uint8 codes")
+    if scale.dtype != torch.float16 or bias.dtype != torch.float16:
+        raise TypeError("fp16 scale and bias")
+    rows = S_src if rows is None else int(rows)
+    rc = lib().gqa_attn_quantize_q4(_ptr(src), S_src, _ptr(codes), _ptr(scale), _ptr(bias), codes.shape[2],
+                                    int(dst_row0), B * Hkv, rows, D, int(group_size), _stream(stream))
+    _check(rc, "gqa_attn_quantize_q4")
 
 
 def gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len) -> int:

@@ -65,3 +65,10 @@ def prefill_flops(Hq, D, q_len, kv_len, causal=True, batch=1):
 def score_matrix_bytes(Hq, q_len, kv_len, elem_bytes):
     """Bytes of the [Hq, q_len, kv_len] score matrix the unfused path writes."""
     return Hq * q_len * kv_len * elem_bytes
+
+
+def quantize_bytes(rows: int, D: int, group_size: int = 64) -> int:
+    """Bytes moved by 4-bit quantization of `rows` bf16 rows: each row is read
+    (2*D bytes) and written as D/2 code bytes plus an fp16 scale and bias per
+    group."""
+    return rows * (2 * D + D // 2 + 4 * (D // group_size))

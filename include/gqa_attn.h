@@ -150,6 +150,38 @@ GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const v
                                        size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * 4-bit group-affine quantization of KV rows (the cache format read by
+ * gqa_attn_decode_q4).
+ *
+ * "Batching Decode Attention Across Requests ...", VeloxQuant-MLX blog,
+ * "Part 4": quantizing the whole growing history every step cost more than
+ * the attention; only the newly aged, group-aligned block of tokens should be
+ * quantized each step.  This call quantizes rows [0, rows) of every head of
+ * `src` into rows [dst_row0, dst_row0 + rows) of every head of the cache: a
+ * whole cache after prefill, or one flushed block per decode step.
+ *
+ *   src     bf16 [heads, src_head_rows, D]      (heads = B * Hkv)
+ *   codes   uint8 [heads, dst_head_rows, D/2]   element 2t in the low nibble
+ *                                               of byte t (written)
+ *   scale,  fp16 [heads, dst_head_rows, D/64]   (written)
+ *   bias
+ * Per group of group_size = 64 elements along D: scale = fp16((max - min) /
+ * 15), bias = fp16(min), r = fp32(1 / scale), code = clamp(round_half_even(
+ * (x - bias) * r), 0, 15), code 0 when scale == 0, in IEEE fp32 with
+ * round-to-nearest operations: the codes are a deterministic function of the
+ * input.  The pages give the format
+ * x = code * scale + bias but no quantizer; this is the library's reading.
+ * Rows of the cache outside [dst_row0, dst_row0 + rows) are not touched.
+ * D in {64, 128}; src 16-byte and codes 4-byte aligned, scale and bias
+ * 2-byte aligned; rows <= src_head_rows, dst_row0 + rows <= dst_head_rows.
+ * Errors as for decode.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_head_rows, uint8_t* codes,
+                                      uint16_t* scale, uint16_t* bias, int64_t dst_head_rows,
+                                      int64_t dst_row0, int heads, int rows, int D, int group_size,
+                                      void* stream);
+
+/* ---------------------------------------------------------------------------
  * Single-token decode without any caller-provided or allocated scratch.
  *
  * There is no counterpart of this entry point in the pages; it exists for

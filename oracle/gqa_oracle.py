@@ -35,9 +35,10 @@ design notes):
     dequantises them and calls SDPA -- this module is that baseline);
   * the 4-bit quantizer (the pages say "group-affine", x = code*scale + bias,
     and give no quantizer): per group, scale = fp16((max - min) / 15),
-    bias = fp16(min), code = clamp(round_half_even((x - bias) / scale), 0,
-    15), code 0 when scale == 0; computed in float32, the precision in which
-    the GPU kernel takes the same integer decisions;
+    bias = fp16(min), r = fp32(1 / scale), code = clamp(round_half_even((x -
+    bias) * r), 0, 15), code 0 when scale == 0; computed in float32, the
+    precision in which the GPU kernel takes the same integer decisions (one
+    reciprocal per group rather than a division per element);
   * a paged cache (the pages name paged attention but give no layout): a
     pool [num_blocks, Hkv, block_size, D] and an integer block table
     [B, max_blocks]; key row j of request b is row j % block_size of block
@@ -231,8 +232,8 @@ def quantize_q4(x, group_size: int = 64):
 
     Per group of ``group_size`` consecutive elements along D: the minimum and
     maximum m, M; scale = fp16((M - m) / 15) and bias = fp16(m) (round to
-    nearest); code = round-half-even((x - bias) / scale) clamped to [0, 15],
-    and 0 where the scale is 0.  Codes are packed two per byte, element 2t in
+    nearest); r = 1 / scale rounded to float32; code = round-half-even((x -
+    bias) * r) clamped to [0, 15], and 0 where the scale is 0.  Codes are packed two per byte, element 2t in
     the low nibble of byte t.  Returns (codes uint8 [..., D/2], scale fp16,
     bias fp16 [..., D/group_size]).  ("Batching Decode Attention Across
     Requests ...", VeloxQuant-MLX blog, "Part 4": the cache is quantized
@@ -250,7 +251,8 @@ def quantize_q4(x, group_size: int = 64):
     s32 = scale.astype(np.float32)[..., None]
     b32 = bias.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
-        q = np.rint((grp - b32) / s32)
+        r32 = np.float32(1.0) / s32
+        q = np.rint((grp - b32) * r32)
     q = np.where(s32 > 0, np.clip(q, 0, 15), 0).astype(np.uint8).reshape(x.shape)
     packed = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
     return packed, scale, bias

@@ -42,3 +42,10 @@ def test_chunk_flops():
 def test_q4_row_bytes():
     # 64 bytes of codes + 2 groups x (fp16 scale + fp16 bias) = 72 B per row
     assert metrics.q4_row_bytes(128, 64) == 72
+
+
+def test_quantize_bytes_per_row():
+    # a D=128 bf16 row is read (256 B) and written as 64 code bytes plus two
+    # fp16 (scale, bias) pairs: 256 + 64 + 8
+    assert metrics.quantize_bytes(1, 128) == 328
+    assert metrics.quantize_bytes(10, 64) == 10 * (128 + 32 + 4)

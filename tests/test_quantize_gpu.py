@@ -1,0 +1,111 @@
+"""The GPU 4-bit quantizer against the oracle's, bit for bit.
+
+Codes are integers decided in fp32 and scale/bias are fp16 roundings, so the
+comparison is exact (no tolerance): same codes, same scale and bias bits.
+Rows of the cache outside the destination range must keep their contents.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_attention_kv_decode_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def empty_cache(B, Hkv, S_cap, D, fill=0xA5):
+    codes = torch.full((B, Hkv, S_cap, D // 2), fill, dtype=torch.uint8, device=DEV)
+    scale = torch.full((B, Hkv, S_cap, D // 64), 7.0, dtype=torch.float16, device=DEV)
+    bias = torch.full((B, Hkv, S_cap, D // 64), -7.0, dtype=torch.float16, device=DEV)
+    return codes, scale, bias
+
+
+def check_rows(src, codes, scale, bias, dst_row0):
+    n = src.shape[2]
+    c, s, b = oracle.quantize_q4(src.float().cpu().numpy())
+    np.testing.assert_array_equal(codes[:, :, dst_row0:dst_row0 + n].cpu().numpy(), c)
+    np.testing.assert_array_equal(scale[:, :, dst_row0:dst_row0 + n].cpu().view(torch.int16).numpy(),
+                                  torch.from_numpy(s).view(torch.int16).numpy())
+    np.testing.assert_array_equal(bias[:, :, dst_row0:dst_row0 + n].cpu().view(torch.int16).numpy(),
+                                  torch.from_numpy(b).view(torch.int16).numpy())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("S", [1, 7, 64, 1000])
+@pytest.mark.parametrize("mag", [1.0, 1e-3, 300.0])
+def test_quantizer_matches_oracle_bit_for_bit(D, S, mag):
+    x = (inputs.randn((2, 8, S, D), 71 + S, torch.float32, DEV) * mag).to(torch.bfloat16)
+    codes, scale, bias = empty_cache(2, 8, S + 5, D)
+    binding.gqa_attn_quantize_q4(x, codes, scale, bias, dst_row0=3)
+    torch.cuda.synchronize()
+    check_rows(x, codes, scale, bias, 3)
+    # rows outside [3, 3 + S) are untouched
+    assert (codes[:, :, :3] == 0xA5).all() and (codes[:, :, 3 + S:] == 0xA5).all()
+    assert (scale[:, :, :3] == 7.0).all() and (bias[:, :, 3 + S:] == -7.0).all()
+
+
+def test_quantizer_hand_cases_on_the_gpu():
+    with open(GOLDEN) as f:
+        cases = json.load(f)["quantizer_cases"]
+    x = torch.tensor([c["x"] for c in cases], dtype=torch.float32).to(torch.bfloat16).view(1, len(cases), 1, 64).to(DEV)
+    codes, scale, bias = empty_cache(1, len(cases), 1, 64)
+    binding.gqa_attn_quantize_q4(x, codes, scale, bias)
+    torch.cuda.synchronize()
+    for i, c in enumerate(cases):
+        assert codes[0, i, 0].cpu().tolist() == c["codes"], c["name"]
+        assert scale[0, i, 0].float().item() == c["scale"][0]
+        assert bias[0, i, 0].float().item() == c["bias"][0]
+
+
+def test_incremental_flush_equals_one_pass():
+    """Quantizing a cache one aged block of 64 rows at a time (the decode-time
+    flush) gives the same bytes as quantizing it in one call."""
+    S, B, Hkv, D = 640, 4, 8, 128
+    x = inputs.randn((B, Hkv, S, D), 81, torch.bfloat16, DEV)
+    whole = empty_cache(B, Hkv, S, D)
+    binding.gqa_attn_quantize_q4(x, *whole)
+    parts = empty_cache(B, Hkv, S, D, fill=0x11)
+    for r0 in range(0, S, 64):
+        binding.gqa_attn_quantize_q4(x[:, :, r0:r0 + 64].contiguous(), *parts, dst_row0=r0)
+    torch.cuda.synchronize()
+    for a, b in zip(whole, parts):
+        assert torch.equal(a, b)
+
+
+def test_decode_over_the_gpu_quantized_cache():
+    """q4 decode on a cache the GPU quantized matches the oracle on the oracle's codes."""
+    B, Hq, Hkv, D, S = 4, 32, 8, 128, 2048
+    k = inputs.randn((B, Hkv, S, D), 91, torch.bfloat16, DEV)
+    v = inputs.randn((B, Hkv, S, D), 92, torch.bfloat16, DEV)
+    q = inputs.randn((B, Hq, 1, D), 93, torch.bfloat16, DEV)
+    kc, ks, kb = empty_cache(B, Hkv, S, D)
+    vc, vs, vb = empty_cache(B, Hkv, S, D)
+    binding.gqa_attn_quantize_q4(k, kc, ks, kb)
+    binding.gqa_attn_quantize_q4(v, vc, vs, vb)
+    o = binding.decode_q4(q, kc, ks, kb, vc, vs, vb)
+    torch.cuda.synchronize()
+    okc, oks, okb = oracle.quantize_q4(k.float().cpu().numpy())
+    ovc, ovs, ovb = oracle.quantize_q4(v.float().cpu().numpy())
+    ref = oracle.attention_q4(q.float().cpu().numpy(), okc, oks, okb, ovc, ovs, ovb, scale=D ** -0.5)["o"]
+    assert np.abs(o.float().cpu().numpy() - ref).max() <= 2e-2
+
+
+def test_quantizer_rejects_bad_ranges():
+    x = inputs.randn((1, 2, 8, 128), 5, torch.bfloat16, DEV)
+    codes, scale, bias = empty_cache(1, 2, 8, 128)
+    with pytest.raises(binding.GqaAttnError) as e:
+        binding.gqa_attn_quantize_q4(x, codes, scale, bias, dst_row0=1)  # 1 + 8 rows > 8
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
