@@ -16,4 +16,5 @@ from .gqa_oracle import (  # noqa: F401
     append_paged,
     attention_paged,
     quantize_q4,
+    attention_q4_residual,
 )

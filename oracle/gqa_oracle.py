@@ -39,6 +39,11 @@ design notes):
     bias) * r), 0, 15), code 0 when scale == 0; computed in float32, the
     precision in which the GPU kernel takes the same integer decisions (one
     reciprocal per group rather than a division per element);
+  * the residual window of a 4-bit cache (the pages: a production KIVI cache
+    keeps the most recent tokens unquantized): key rows [0, n_quant[b]) of
+    request b come from the 4-bit cache and rows [n_quant[b], kv_lens[b])
+    from rows [0, kv_lens[b] - n_quant[b]) of the residual buffer, which is
+    kept in the activation dtype (bf16 here);
   * a paged cache (the pages name paged attention but give no layout): a
     pool [num_blocks, Hkv, block_size, D] and an integer block table
     [B, max_blocks]; key row j of request b is row j % block_size of block
@@ -256,3 +261,30 @@ def quantize_q4(x, group_size: int = 64):
     q = np.where(s32 > 0, np.clip(q, 0, 15), 0).astype(np.uint8).reshape(x.shape)
     packed = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
     return packed, scale, bias
+
+
+def attention_q4_residual(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, k_res, v_res,
+                          n_quant, kv_lens, scale=None, group_size: int = 64):
+    """Decode attention over a 4-bit cache followed by an unquantized window.
+
+    Key row j < n_quant[b] of request b is the dequantised row j of the 4-bit
+    cache; key row n_quant[b] + i (i < kv_lens[b] - n_quant[b]) is row i of
+    k_res / v_res [B, Hkv, R_cap, D].  The rows are concatenated, then the
+    attention definition applies.
+    """
+    kq = dequant_q4(k_codes, k_scale, k_bias, group_size)
+    vq = dequant_q4(v_codes, v_scale, v_bias, group_size)
+    kr, vr = _f64(k_res), _f64(v_res)
+    B, hkv, _, D = kq.shape
+    S = max(1, int(max(kv_lens)))
+    k = np.zeros((B, hkv, S, D))
+    v = np.zeros((B, hkv, S, D))
+    for b in range(B):
+        nq, L = int(n_quant[b]), int(kv_lens[b])
+        if not 0 <= nq <= L:
+            raise ValueError("need 0 <= n_quant <= kv_len")
+        k[b, :, :nq] = kq[b, :, :nq]
+        v[b, :, :nq] = vq[b, :, :nq]
+        k[b, :, nq:L] = kr[b, :, :L - nq]
+        v[b, :, nq:L] = vr[b, :, :L - nq]
+    return attention(q, k, v, kv_lens=kv_lens, scale=scale)

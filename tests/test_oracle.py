@@ -442,3 +442,82 @@ def test_pins_catch_quantizer_slips(monkeypatch):
     c, _, _ = oracle.quantize_q4(np.array(case["x"], dtype=np.float32))
     swapped = ((c & 15) << 4) | (c >> 4)
     assert not np.array_equal(swapped, np.array(case["codes"], dtype=np.uint8))
+
+
+# --- 4-bit cache with an unquantized residual window ------------------------------
+
+@pytest.mark.parametrize("case", _cases()["residual_cases"], ids=lambda c: c["name"])
+def test_hand_residual_cases(case):
+    f16 = lambda a: np.array(a, dtype=np.float16)
+    out = oracle.attention_q4_residual(
+        np.array(case["q"]), np.array(case["k_codes"], dtype=np.uint8), f16(case["k_scale"]), f16(case["k_bias"]),
+        np.array(case["v_codes"], dtype=np.uint8), f16(case["v_scale"]), f16(case["v_bias"]),
+        np.array(case["k_res"]), np.array(case["v_res"]), case["n_quant"], case["kv_lens"], scale=case["scale"])
+    np.testing.assert_allclose(out["o"], np.array(case["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["lse"], np.array(case["lse"]), rtol=0, atol=1e-12)
+
+
+def _q4_and_residual(B, Hkv, S, R, D, seed):
+    from gqa_attention_kv_decode_gb300 import inputs
+    kc, ks, kb, vc, vs, vb = (t.numpy() for t in inputs.q4_cache(B, Hkv, D, S, layer=seed))
+    kr = inputs.randn((B, Hkv, R, D), 900 + seed, torch.bfloat16).float().numpy()
+    vr = inputs.randn((B, Hkv, R, D), 901 + seed, torch.bfloat16).float().numpy()
+    return kc, ks, kb, vc, vs, vb, kr, vr
+
+
+def test_residual_window_reduces_to_the_two_parts():
+    """All keys quantized: the q4 oracle.  No key quantized: plain attention on
+    the residual window."""
+    B, Hq, Hkv, S, R, D = 2, 8, 2, 40, 16, 64
+    kc, ks, kb, vc, vs, vb, kr, vr = _q4_and_residual(B, Hkv, S, R, D, 1)
+    q = _rand((B, Hq, 1, D), 77)
+    lens = [40, 9]
+    got = oracle.attention_q4_residual(q, kc, ks, kb, vc, vs, vb, kr, vr, lens, lens)
+    want = oracle.attention_q4(q, kc, ks, kb, vc, vs, vb, kv_lens=lens)
+    np.testing.assert_allclose(got["o"], want["o"], rtol=0, atol=1e-12)
+    lens = [16, 3]
+    got = oracle.attention_q4_residual(q, kc, ks, kb, vc, vs, vb, kr, vr, [0, 0], lens)
+    want = oracle.attention(q, kr, vr, kv_lens=lens)
+    np.testing.assert_allclose(got["o"], want["o"], rtol=0, atol=1e-12)
+
+
+def test_residual_flush_moves_a_block_without_changing_the_keys():
+    """Flushing the oldest block of the window into the 4-bit cache (as
+    dequantised values) leaves the attended key set, hence the output, the
+    same: a row is either in the cache or in the window, never both."""
+    B, Hq, Hkv, S, R, D = 1, 4, 1, 64, 32, 64
+    kc, ks, kb, vc, vs, vb, kr, vr = _q4_and_residual(B, Hkv, S, R, D, 2)
+    q = _rand((B, Hq, 1, D), 78)
+    # window holds rows 20..43 of the sequence; then rows 20..35 move to the cache
+    nq, L = 20, 44
+    before = oracle.attention_q4_residual(q, kc, ks, kb, vc, vs, vb, kr, vr, [nq], [L])
+    kc2, ks2, kb2, vc2, vs2, vb2 = (a.copy() for a in (kc, ks, kb, vc, vs, vb))
+    kq, ksq, kbq = oracle.quantize_q4(kr[:, :, :16])
+    vq, vsq, vbq = oracle.quantize_q4(vr[:, :, :16])
+    kc2[:, :, nq:nq + 16], ks2[:, :, nq:nq + 16], kb2[:, :, nq:nq + 16] = kq, ksq, kbq
+    vc2[:, :, nq:nq + 16], vs2[:, :, nq:nq + 16], vb2[:, :, nq:nq + 16] = vq, vsq, vbq
+    kr2 = np.zeros_like(kr)
+    vr2 = np.zeros_like(vr)
+    kr2[:, :, :L - nq - 16] = kr[:, :, 16:L - nq]
+    vr2[:, :, :L - nq - 16] = vr[:, :, 16:L - nq]
+    after = oracle.attention_q4_residual(q, kc2, ks2, kb2, vc2, vs2, vb2, kr2, vr2, [nq + 16], [L])
+    # the same keys, except that the flushed rows are now quantized: compare
+    # against the window with those rows replaced by their dequantised values
+    kr3, vr3 = kr.copy(), vr.copy()
+    kr3[:, :, :16] = oracle.dequant_q4(kq, ksq, kbq)
+    vr3[:, :, :16] = oracle.dequant_q4(vq, vsq, vbq)
+    ref = oracle.attention_q4_residual(q, kc, ks, kb, vc, vs, vb, kr3, vr3, [nq], [L])
+    np.testing.assert_allclose(after["o"], ref["o"], rtol=0, atol=1e-12)
+    assert not np.allclose(after["o"], before["o"], atol=1e-9)  # quantizing changed the values
+
+
+def test_pins_catch_residual_offset_slip(monkeypatch):
+    real = gqa_oracle.attention_q4_residual
+
+    def off_by_one(q, kc, ks, kb, vc, vs, vb, kr, vr, n_quant, kv_lens, scale=None, group_size=64):
+        return real(q, kc, ks, kb, vc, vs, vb, kr, vr, [max(0, int(n) - 1) for n in n_quant], kv_lens,
+                    scale=scale, group_size=group_size)
+    monkeypatch.setattr(oracle, "attention_q4_residual", off_by_one)
+    with pytest.raises(AssertionError):
+        for case in _cases()["residual_cases"]:
+            test_hand_residual_cases(case)
