@@ -323,6 +323,49 @@ def paged_point(binding, B, device, stream, flush, iters=10, block_size=64):
             "GBps": round(nbytes / us / 1e3, 1)}
 
 
+def q4_residual_point(binding, S, device, stream, flush, iters=10, window=100, R_cap=128):
+    """q4 decode (Hq=32, Hkv=8, D=128, B=4, 36 layers) with `window` further
+    tokens in a bf16 residual window: S quantized keys + the window."""
+    B, n_layers = 4, 36
+    layers = []
+    for l in range(n_layers):
+        cache = inputs.q4_cache(B, 8, 128, S, layer=l, device=device)
+        kr = inputs.randn((B, 8, R_cap, 128), inputs.tensor_seed(l, 5), torch.bfloat16, device)
+        vr = inputs.randn((B, 8, R_cap, 128), inputs.tensor_seed(l, 6), torch.bfloat16, device)
+        q = inputs.randn((B, 32, 1, 128), inputs.tensor_seed(l, 0), torch.bfloat16, device)
+        layers.append((q, cache, kr, vr))
+    outs = [torch.empty_like(x[0]) for x in layers]
+    nq = torch.full((B,), S, dtype=torch.int32, device=device)
+    lens = torch.full((B,), S + window, dtype=torch.int32, device=device)
+    ws = torch.zeros(binding.gqa_attn_decode_q4_residual_workspace_size(B, 32, 8, 128, S), dtype=torch.uint8,
+                     device=device)
+    torch.cuda.synchronize()
+
+    def step():
+        for (q, cache, kr, vr), o in zip(layers, outs):
+            binding.gqa_attn_decode_q4_residual(q, *cache, kr, vr, nq, lens, o, 128 ** -0.5, ws, max_quant=S,
+                                                stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    ts = []
+    for _ in range(iters):
+        with torch.cuda.stream(stream):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n_layers)
+    us = statistics.median(ts)
+    nbytes = metrics.q4_decode_bytes(32, 8, 128, [S] * B) + 2 * B * 8 * window * 128 * 2
+    del layers, outs
+    torch.cuda.empty_cache()
+    return {"S_quantized": S, "window": window, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
+
+
 def quantize_point(binding, device, stream, flush, iters=10):
     """4-bit quantization of KV rows (Hkv=8, D=128, B=4): a whole 16384-token K
     cache in one call (HBM-bound), and the per-step flush of one aged block of
@@ -797,6 +840,8 @@ def main():
         line["paged_decode_qwen3_4b_36_layers"] = [paged_point(binding, B, device, stream, flush)
                                                    for B in (16, 64)]
         line["quantize_q4_qwen3_4b"] = quantize_point(binding, device, stream, flush)
+        line["q4_residual_decode_qwen3_4b_B4_36_layers"] = [q4_residual_point(binding, S, device, stream, flush)
+                                                            for S in (2048, 16384)]
         pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
         pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
         line["prefill_causal_qwen05b_bf16"] = pf

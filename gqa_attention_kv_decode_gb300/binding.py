@@ -40,6 +40,8 @@ EXPORTED = (
     "gqa_attn_decode_noalloc",
     "gqa_attn_decode_paged",
     "gqa_attn_quantize_q4",
+    "gqa_attn_decode_q4_residual_workspace_size",
+    "gqa_attn_decode_q4_residual",
     "gqa_attn_decode_q4_workspace_size",
     "gqa_attn_decode_q4",
     "gqa_attn_prefill",
@@ -83,6 +85,11 @@ def lib() -> ctypes.CDLL:
     i64 = ctypes.c_int64
     L.gqa_attn_quantize_q4.argtypes = [vp, i64, vp, vp, vp, i64, i64, i32, i32, i32, i32, vp]
     L.gqa_attn_quantize_q4.restype = i32
+    L.gqa_attn_decode_q4_residual_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.gqa_attn_decode_q4_residual_workspace_size.restype = sz
+    L.gqa_attn_decode_q4_residual.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+    L.gqa_attn_decode_q4_residual.restype = i32
     L.gqa_attn_decode_q4_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.gqa_attn_decode_q4_workspace_size.restype = sz
     L.gqa_attn_decode_q4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -206,6 +213,30 @@ def gqa_attn_quantize_q4(src, codes, scale, bias, dst_row0=0, rows=None, group_s
     _check(rc, "gqa_attn_quantize_q4")
 
 
+def gqa_attn_decode_q4_residual_workspace_size(B, Hq, Hkv, D, max_quant) -> int:
+    return lib().gqa_attn_decode_q4_residual_workspace_size(B, Hq, Hkv, D, max_quant)
+
+
+def gqa_attn_decode_q4_residual(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, k_res, v_res,
+                                n_quant, kv_lens, o, scale, workspace, max_quant=None, group_size=64,
+                                stream=None):
+    """4-bit cache rows [0, n_quant[b]) then window rows (bf16 k_res, v_res
+    [B,Hkv,R_cap,D]) up to kv_lens[b]; q, o bf16 [B,Hq,1,D]."""
+    B, Hq, Tq, D = q.shape
+    Hkv, S_cap = k_codes.shape[1], k_codes.shape[2]
+    R_cap = k_res.shape[2]
+    if q.dtype != torch.bfloat16 or k_res.dtype != torch.bfloat16:
+        raise TypeError("bf16 q and window")
+    max_quant = S_cap if max_quant is None else int(max_quant)
+    rc = lib().gqa_attn_decode_q4_residual(_ptr(q), _ptr(k_codes), _ptr(k_scale), _ptr(k_bias),
+                                           _ptr(v_codes), _ptr(v_scale), _ptr(v_bias), _ptr(k_res),
+                                           _ptr(v_res), _ptr(n_quant), _ptr(kv_lens), _ptr(o), B, Hq, Hkv,
+                                           D, S_cap, R_cap, max_quant, int(group_size), float(scale),
+                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream(stream))
+    _check(rc, "gqa_attn_decode_q4_residual")
+
+
 def gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len) -> int:
     return lib().gqa_attn_decode_q4_workspace_size(B, Hq, Hkv, D, max_kv_len)
 
@@ -283,6 +314,24 @@ def decode(q, k, v, kv_lens=None, scale=None, max_kv_len=None, workspace=None, s
         workspace = decode_workspace(B, Hq, Hkv, D, max_kv_len, _dtype_code(q), q.device)
     o = torch.empty_like(q)
     gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len, stream)
+    return o
+
+
+def decode_q4_residual(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, k_res, v_res, n_quant,
+                       kv_lens, max_quant=None, scale=None, workspace=None, stream=None):
+    B, Hq, _, D = q.shape
+    Hkv, S_cap = k_codes.shape[1], k_codes.shape[2]
+    max_quant = S_cap if max_quant is None else int(max_quant)
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        n = gqa_attn_decode_q4_residual_workspace_size(B, Hq, Hkv, D, max_quant)
+        if n == 0:
+            raise ValueError("invalid decode shape")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    gqa_attn_decode_q4_residual(q, k_codes, k_scale, k_bias, v_codes, v_scale, v_bias, k_res, v_res,
+                                n_quant, kv_lens, o, scale, workspace, max_quant, stream=stream)
     return o
 
 

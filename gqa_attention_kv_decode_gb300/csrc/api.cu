@@ -303,6 +303,83 @@ GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes, const
   return GQA_OK;
 }
 
+GQA_ATTN_API size_t gqa_attn_decode_q4_residual_workspace_size(int B, int Hq, int Hkv, int D,
+                                                               int max_quant) {
+  if (check_decode_shape(B, Hq, Hkv, D, max_quant, max_quant, 1.f) != GQA_OK) return 0;
+  const SplitPlan p = plan_splits(B, Hq, Hkv, max_quant, decode_q4_tile_rows(D), device_sm_count(),
+                                  decode_q4_ctas_per_sm());
+  return workspace_layout(B, Hq, Hkv, p.n_hc, p.n_split + 1, D).total;
+}
+
+GQA_ATTN_API int gqa_attn_decode_q4_residual(
+    const void* q, const uint8_t* k_codes, const uint16_t* k_scale, const uint16_t* k_bias,
+    const uint8_t* v_codes, const uint16_t* v_scale, const uint16_t* v_bias, const void* k_res,
+    const void* v_res, const int32_t* n_quant, const int32_t* kv_lens, void* o, int B, int Hq, int Hkv,
+    int D, int S_cap, int R_cap, int max_quant, int group_size, float scale, void* workspace,
+    size_t ws_bytes, void* stream) {
+  int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_quant, scale);
+  if (rc != GQA_OK) return rc;
+  if (R_cap < 1 || group_size != 64 || D % group_size != 0) return GQA_ERR_INVALID_ARG;
+  if (S_cap % 8 != 0) return GQA_ERR_INVALID_ARG;  // scale/bias tiles are copied in 16-byte pieces
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  rc = check_ptrs({q, k_codes, v_codes, k_scale, k_bias, v_scale, v_bias, o, k_res, v_res}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  rc = check_ptrs({n_quant, kv_lens}, dev, 4);
+  if (rc != GQA_OK) return rc;
+  if (workspace == nullptr) return GQA_ERR_WORKSPACE;
+  rc = check_ptrs({workspace}, dev, 256);
+  if (rc == GQA_ERR_INVALID_ARG) return GQA_ERR_WORKSPACE;
+  if (rc != GQA_OK) return rc;
+
+  DecodeQ4Args aq;
+  aq.q = q;
+  aq.k_codes = k_codes;
+  aq.k_scale = k_scale;
+  aq.k_bias = k_bias;
+  aq.v_codes = v_codes;
+  aq.v_scale = v_scale;
+  aq.v_bias = v_bias;
+  aq.o = o;
+  aq.kv_lens = n_quant;
+  aq.B = B;
+  aq.Hq = Hq;
+  aq.Hkv = Hkv;
+  aq.D = D;
+  aq.S_cap = S_cap;
+  aq.max_kv_len = max_quant;
+  aq.scale = scale;
+  aq.workspace = workspace;
+  aq.plan = plan_splits(B, Hq, Hkv, max_quant, decode_q4_tile_rows(D), device_sm_count(),
+                        decode_q4_ctas_per_sm());
+  if (ws_bytes < workspace_layout(B, Hq, Hkv, aq.plan.n_hc, aq.plan.n_split + 1, D).total)
+    return GQA_ERR_WORKSPACE;
+
+  DecodeArgs ar;  // the window: bf16 [B, Hkv, R_cap, D], one split per (request, head chunk)
+  ar.q = q;
+  ar.k = k_res;
+  ar.v = v_res;
+  ar.o = o;
+  ar.kv_lens = kv_lens;
+  ar.B = B;
+  ar.Hq = Hq;
+  ar.Hkv = Hkv;
+  ar.D = D;
+  ar.S_cap = R_cap;
+  ar.max_kv_len = R_cap;
+  ar.scale = scale;
+  ar.dtype = GQA_BF16;
+  ar.workspace = workspace;
+  ar.plan = aq.plan;
+  ar.plan.tile = decode_tile_rows(GQA_BF16, D);
+  ar.plan.chunk = ((R_cap + ar.plan.tile - 1) / ar.plan.tile) * ar.plan.tile;
+  ar.plan.n_split = 1;
+  const cudaError_t e = launch_decode_q4_residual(aq, ar, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
 GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, void* o, int B,
                                   int Hq, int Hkv, int D, int q_len, int kv_len, int S_cap,
                                   float scale, int causal, int dtype, void* stream) {

@@ -56,6 +56,13 @@ struct MmaParams {
   const __nv_bfloat16* v_new;
   unsigned char* k_pool;       // pool bases, written by the append
   unsigned char* v_pool;
+  // residual window after a 4-bit cache (len_sub != nullptr): the request
+  // attends rows [0, kv_lens[b] - clamp(len_sub[b], 0, max_sub)) of this
+  // cache, and its partial goes to slot ceil(that clamp / slot_chunk)
+  const int32_t* len_sub;
+  int max_sub, slot_chunk;
+  int n_slots;        // partial slots per (request, head) row
+  int force_partial;  // write a partial even for a one-split request
 };
 
 template <int D, int NSTAGE>
@@ -150,11 +157,22 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
   grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
+  int slot0 = 0;
+  if (p.len_sub != nullptr) {
+    const int nq = p.len_sub[b];
+    const int nqc = nq < 0 ? 0 : (nq > p.max_sub ? p.max_sub : nq);
+    if ((nqc != nq || L < 0) && split == 0 && blockIdx.y == 0 && tid == 0)
+      atomicOr(p.status, GQA_DEV_KVLEN_CLAMPED);
+    slot0 = (nqc + p.slot_chunk - 1) / p.slot_chunk;
+    L = max(L, 0) - nqc;
+    if (L < 0) L = 0;
+  }
   if (L < 0 || L > p.max_kv_len) {
     if (split == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, GQA_DEV_KVLEN_CLAMPED);
     L = L < 0 ? 0 : p.max_kv_len;
   }
   if (L == 0) {  // no visible key: the output row is zeros
+    if (p.force_partial) return;  // (the merge writes it)
     if (split == 0) {
       if (blockIdx.y == 0 && tid == 0) atomicOr(p.status, GQA_DEV_EMPTY_REQUEST);
       for (int e = tid; e < nh * D; e += C::NTHR)
@@ -387,11 +405,11 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
       lt += lw[w * 8 + h] * ew;
       sum += merge_s[(w * 8 + h) * D + d] * ew;
     }
-    if (n_used == 1) {
+    if (n_used == 1 && !p.force_partial) {
       p.o[(ws_row + h) * D + d] = __float2bfloat16_rn(sum / lt);
     } else {
-      p.part_o[((ws_row + h) * p.n_split + split) * D + d] = sum;
-      if (d == 0) p.ml[(ws_row + h) * p.n_split + split] = make_float2(M, lt);
+      p.part_o[((ws_row + h) * p.n_slots + slot0 + split) * D + d] = sum;
+      if (d == 0) p.ml[(ws_row + h) * p.n_slots + slot0 + split] = make_float2(M, lt);
     }
   }
 }
@@ -475,7 +493,8 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.chunk = a.plan.chunk;
   p.n_split = a.plan.n_split;
   p.qscale = float(double(a.scale) * 1.4426950408889634);
-  const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, a.plan.n_split, a.D);
+  const WorkspaceLayout w =
+      workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, a.n_slots > 0 ? a.n_slots : a.plan.n_split, a.D);
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
@@ -489,10 +508,31 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
   p.k_pool = static_cast<unsigned char*>(const_cast<void*>(a.k));
   p.v_pool = static_cast<unsigned char*>(const_cast<void*>(a.v));
+  p.len_sub = a.len_sub;
+  p.max_sub = a.max_sub;
+  p.slot_chunk = a.slot_chunk > 0 ? a.slot_chunk : 1;
+  p.n_slots = a.n_slots > 0 ? a.n_slots : a.plan.n_split;
+  p.force_partial = a.force_partial;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   if (paged)
     return a.D == 128 ? launch_mma<128, 3, true>(tk, tv, p, grid, stream) : launch_mma<64, 6, true>(tk, tv, p, grid, stream);
   return a.D == 128 ? launch_mma<128, 3, false>(tk, tv, p, grid, stream) : launch_mma<64, 6, false>(tk, tv, p, grid, stream);
+}
+
+}  // namespace gqa
+
+
+namespace gqa {
+
+cudaError_t launch_decode_mma_residual(const DecodeArgs& a, const int32_t* n_quant, int max_quant, int slot_chunk,
+                                       int n_slots, cudaStream_t stream) {
+  DecodeArgs r = a;
+  r.len_sub = n_quant;
+  r.max_sub = max_quant;
+  r.slot_chunk = slot_chunk;
+  r.n_slots = n_slots;
+  r.force_partial = 1;
+  return launch_decode_mma(r, stream);
 }
 
 }  // namespace gqa

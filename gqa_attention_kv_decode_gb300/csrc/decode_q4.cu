@@ -63,6 +63,8 @@ struct Q4Params {
   float2* ml;
   float* part_o;
   uint64_t wait_limit_ns;
+  int n_slots;        // partial slots per (request, head) row in the workspace
+  int force_partial;  // write partials even for a one-split request (a residual window follows)
 };
 
 template <int D, int NSTAGE>
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
     L = L < 0 ? 0 : p.max_kv_len;
   }
   if (L == 0) {  // no visible key: the output row is zeros
+    if (p.force_partial) return;  // no 4-bit keys: the window (or the merge) has the row
     if (split == 0) {
       if (blockIdx.y == 0 && tid == 0) atomicOr(p.status, GQA_DEV_EMPTY_REQUEST);
       for (int e = tid; e < nh * D; e += C::NTHR)
@@ -586,11 +589,11 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
       lt += lw[w * 8 + h] * ew;
       sum += merge_s[(w * 8 + h) * D + d] * ew;
     }
-    if (n_used == 1) {
+    if (n_used == 1 && !p.force_partial) {
       p.o[(ws_row + h) * D + d] = __float2bfloat16_rn(sum / lt);
     } else {
-      p.part_o[((ws_row + h) * p.n_split + split) * D + d] = sum;
-      if (d == 0) p.ml[(ws_row + h) * p.n_split + split] = make_float2(M, lt);
+      p.part_o[((ws_row + h) * p.n_slots + split) * D + d] = sum;
+      if (d == 0) p.ml[(ws_row + h) * p.n_slots + split] = make_float2(M, lt);
     }
   }
 }
@@ -644,8 +647,10 @@ cudaError_t launch_decode_q4(const DecodeQ4Args& a, cudaStream_t stream) {
   p.max_kv_len = a.max_kv_len;
   p.chunk = a.plan.chunk;
   p.n_split = a.plan.n_split;
+  p.n_slots = a.n_slots > 0 ? a.n_slots : a.plan.n_split;
+  p.force_partial = a.force_partial;
   p.qscale = float(double(a.scale) * 1.4426950408889634);
-  const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, a.plan.n_split, a.D);
+  const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, p.n_slots, a.D);
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
@@ -654,7 +659,7 @@ cudaError_t launch_decode_q4(const DecodeQ4Args& a, cudaStream_t stream) {
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   cudaError_t e = a.D == 128 ? launch_q4_mma<128, kQ4Stages128>(p, grid, stream)
                              : launch_q4_mma<64, kQ4Stages64>(p, grid, stream);
-  if (e != cudaSuccess || a.plan.n_split == 1) return e;
+  if (e != cudaSuccess || a.plan.n_split == 1 || a.force_partial) return e;
   MergeParams m;
   m.o = p.o;
   m.kv_lens = p.kv_lens;
@@ -664,6 +669,46 @@ cudaError_t launch_decode_q4(const DecodeQ4Args& a, cudaStream_t stream) {
   m.n_split = p.n_split;
   m.ml = p.ml;
   m.part_o = p.part_o;
+  const int rows = a.B * a.Hq;
+  return a.D == 128 ? launch_merge<__nv_bfloat16, 128>(m, rows, stream)
+                    : launch_merge<__nv_bfloat16, 64>(m, rows, stream);
+}
+
+}  // namespace gqa
+
+
+namespace gqa {
+
+// A 4-bit cache followed by an unquantized (bf16) residual window: the window
+// kernel (decode_mma.cu) writes one partial per row into the slot after the
+// 4-bit splits, the 4-bit kernel writes all its splits as partials, and the
+// merge combines them.  Launch order: window, 4-bit splits, merge (each
+// waits for the previous grid; the window grid is small, and the 4-bit
+// grid's L2 prefetch overlaps it).
+cudaError_t launch_decode_q4_residual(const DecodeQ4Args& aq, const DecodeArgs& ar, cudaStream_t stream) {
+  const int n_slots = aq.plan.n_split + 1;
+  cudaError_t e = launch_decode_mma_residual(ar, aq.kv_lens, aq.max_kv_len, aq.plan.chunk, n_slots, stream);
+  if (e != cudaSuccess) return e;
+  DecodeQ4Args a = aq;
+  a.n_slots = n_slots;
+  a.force_partial = 1;
+  e = launch_decode_q4(a, stream);
+  if (e != cudaSuccess) return e;
+  const WorkspaceLayout w = workspace_layout(a.B, a.Hq, a.Hkv, a.plan.n_hc, n_slots, a.D);
+  unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+  MergeParams m;
+  m.o = a.o;
+  m.kv_lens = ar.kv_lens;
+  m.Hq = a.Hq;
+  m.max_kv_len = a.max_kv_len;
+  m.chunk = a.plan.chunk;
+  m.n_split = n_slots;
+  m.ml = reinterpret_cast<const float2*>(ws + w.off_ml);
+  m.part_o = reinterpret_cast<const float*>(ws + w.off_o);
+  m.n_quant = aq.kv_lens;
+  m.max_quant = aq.max_kv_len;
+  m.res_cap = ar.max_kv_len;
+  m.status = reinterpret_cast<uint32_t*>(ws);
   const int rows = a.B * a.Hq;
   return a.D == 128 ? launch_merge<__nv_bfloat16, 128>(m, rows, stream)
                     : launch_merge<__nv_bfloat16, 64>(m, rows, stream);

@@ -63,6 +63,10 @@ struct DecodeArgs {
   int block_size = 0, max_blocks = 0, num_blocks = 0;
   const void* k_new = nullptr;
   const void* v_new = nullptr;
+  // residual window after a 4-bit cache (bf16 kernel only): see
+  // launch_decode_mma_residual
+  const int32_t* len_sub = nullptr;
+  int max_sub = 0, slot_chunk = 0, n_slots = 0, force_partial = 0;
 };
 
 // Tile height (rows) of the decode kernel for this dtype / head size, and how
@@ -86,7 +90,18 @@ struct DecodeQ4Args {
   float scale;
   void* workspace;
   SplitPlan plan;
+  int n_slots = 0;        // partial slots per row (0: plan.n_split)
+  int force_partial = 0;  // write partials even for one split, and launch no merge
 };
+
+// The residual window of a 4-bit cache: request b attends rows
+// [0, kv_lens[b] - clamp(n_quant[b], 0, max_quant)) of a.k / a.v (bf16,
+// S_cap = the window capacity) and writes its partial into slot
+// ceil(clamp(n_quant[b]) / slot_chunk) of n_slots.
+cudaError_t launch_decode_mma_residual(const DecodeArgs& a, const int32_t* n_quant, int max_quant, int slot_chunk,
+                                       int n_slots, cudaStream_t stream);
+// A 4-bit cache (aq, with aq.kv_lens = n_quant) followed by a bf16 window (ar).
+cudaError_t launch_decode_q4_residual(const DecodeQ4Args& aq, const DecodeArgs& ar, cudaStream_t stream);
 
 int decode_q4_tile_rows(int D);
 int decode_q4_ctas_per_sm();

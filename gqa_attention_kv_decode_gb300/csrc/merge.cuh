@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "gqa_attn.h"
 #include "ptx.cuh"
 
 namespace gqa {
@@ -25,9 +26,16 @@ __device__ __forceinline__ void store_f(__nv_bfloat16* p, float x) { *p = __floa
 struct MergeParams {
   void* o;
   const int32_t* kv_lens;
-  int Hq, max_kv_len, chunk, n_split;
+  int Hq, max_kv_len, chunk, n_split;  // n_split: partial slots per row
   const float2* ml;
   const float* part_o;
+  // 4-bit cache + residual window (n_quant != nullptr): the 4-bit part of
+  // request b has clamp(n_quant[b], 0, max_quant) keys in chunks of `chunk`,
+  // the window clamp(kv_lens[b] - that, 0, res_cap) keys in one more slot;
+  // every used slot holds a partial, even when there is only one.
+  const int32_t* n_quant = nullptr;
+  int max_quant = 0, res_cap = 0;
+  uint32_t* status = nullptr;
 };
 
 // Merges the split partials of one (request, query head) row, after the split
@@ -54,9 +62,27 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
   grid_launch_dependents();  // the next call's split kernel may start staging
   grid_dependency_wait();
   int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
-  L = L < 0 ? 0 : (L > p.max_kv_len ? p.max_kv_len : L);
-  const int n_used = (L + p.chunk - 1) / p.chunk;
-  if (n_used <= 1) return;  // written by the split kernel itself
+  int n_used;
+  if (p.n_quant != nullptr) {
+    L = L < 0 ? 0 : L;
+    int nq = p.n_quant[b];
+    nq = nq < 0 ? 0 : (nq > p.max_quant ? p.max_quant : nq);
+    int lr = L - nq;
+    lr = lr < 0 ? 0 : (lr > p.res_cap ? p.res_cap : lr);
+    n_used = (nq + p.chunk - 1) / p.chunk + (lr > 0 ? 1 : 0);
+    if (n_used == 0) {  // no key at all: zeros
+      if (tid == 0) atomicOr(p.status, GQA_DEV_EMPTY_REQUEST);
+      if (tid < D4) {
+        T* dst = static_cast<T*>(p.o) + size_t(bh) * D + tid * 4;
+        for (int e = 0; e < 4; ++e) store_f(dst + e, 0.f);
+      }
+      return;
+    }
+  } else {
+    L = L < 0 ? 0 : (L > p.max_kv_len ? p.max_kv_len : L);
+    n_used = (L + p.chunk - 1) / p.chunk;
+    if (n_used <= 1) return;  // written by the split kernel itself
+  }
   const float2* ml = p.ml + size_t(bh) * p.n_split;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + size_t(bh) * p.n_split * D) + c4;
   float4 x[PRE];

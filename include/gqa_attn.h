@@ -150,6 +150,41 @@ GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const v
                                        size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode over a 4-bit cache followed by an unquantized residual window.
+ *
+ * "Batching Decode Attention Across Requests ...", VeloxQuant-MLX blog,
+ * "What this means in practice": the benchmark cache had no fp16 residual
+ * window, and a production KIVI cache keeps the most recent tokens
+ * unquantized.  Here the window is kept in bf16 (the dtype of q and o):
+ * key rows [0, n_quant[b]) of request b come from the 4-bit cache (as in
+ * gqa_attn_decode_q4) and key rows [n_quant[b], kv_lens[b]) from rows
+ * [0, kv_lens[b] - n_quant[b]) of the window.  A block that ages out of the
+ * window is moved into the 4-bit cache with gqa_attn_quantize_q4.
+ *
+ *   q, o          bf16 [B, Hq, 1, D]
+ *   codes, scale, as for gqa_attn_decode_q4, [B, Hkv, S_cap, ...]
+ *   bias (K, V)
+ *   k_res, v_res  bf16 [B, Hkv, R_cap, D]
+ *   n_quant       device int32 [B]: 4-bit rows per request, clamped into
+ *                 [0, max_quant] (GQA_DEV_KVLEN_CLAMPED)
+ *   kv_lens       device int32 [B]: all keys per request; the window part
+ *                 kv_lens[b] - n_quant[b] is clamped into [0, R_cap]
+ *   max_quant     host bound of n_quant, 1 <= max_quant <= S_cap
+ * A request with no key at all gets a zero row (GQA_DEV_EMPTY_REQUEST).
+ * Three kernels run (window, 4-bit splits, merge); the workspace size comes
+ * from gqa_attn_decode_q4_residual_workspace_size(B, Hq, Hkv, D, max_quant).
+ * Errors as for gqa_attn_decode_q4.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API size_t gqa_attn_decode_q4_residual_workspace_size(int B, int Hq, int Hkv, int D,
+                                                               int max_quant);
+GQA_ATTN_API int gqa_attn_decode_q4_residual(
+    const void* q, const uint8_t* k_codes, const uint16_t* k_scale, const uint16_t* k_bias,
+    const uint8_t* v_codes, const uint16_t* v_scale, const uint16_t* v_bias, const void* k_res,
+    const void* v_res, const int32_t* n_quant, const int32_t* kv_lens, void* o, int B, int Hq, int Hkv,
+    int D, int S_cap, int R_cap, int max_quant, int group_size, float scale, void* workspace,
+    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * 4-bit group-affine quantization of KV rows (the cache format read by
  * gqa_attn_decode_q4).
  *
