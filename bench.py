@@ -323,6 +323,47 @@ def paged_point(binding, B, device, stream, flush, iters=10, block_size=64):
             "GBps": round(nbytes / us / 1e3, 1)}
 
 
+def layers_point(binding, S, device, stream, flush, iters=10, NL=28):
+    """Qwen2.5-7B head geometry, fp32, B=1: NL layers as NL gqa_attn_decode
+    calls versus one gqa_attn_decode_layers launch over the stacked layers
+    (the pages' cross-layer batching; a microbenchmark of the per-call cost)."""
+    q = inputs.randn((NL, 1, HQ, 1, D), inputs.tensor_seed(0, 0), torch.float32, device)
+    k = inputs.randn((NL, 1, HKV, S, D), inputs.tensor_seed(0, 1), torch.float32, device)
+    v = inputs.randn((NL, 1, HKV, S, D), inputs.tensor_seed(0, 2), torch.float32, device)
+    o = torch.empty_like(q)
+    ws_l = torch.zeros(binding.gqa_attn_decode_layers_workspace_size(NL, 1, HQ, HKV, D, S, binding.GQA_F32),
+                       dtype=torch.uint8, device=device)
+    ws_1 = binding.decode_workspace(1, HQ, HKV, D, S, binding.GQA_F32, device)
+    torch.cuda.synchronize()
+    views = [(q[l], k[l], v[l], o[l]) for l in range(NL)]  # slicing stays out of the timed region
+    seq = lambda: [binding.gqa_attn_decode(ql, kl, vl, ol, None, D ** -0.5, ws_1, max_kv_len=S, stream=stream)
+                   for ql, kl, vl, ol in views]
+    one = lambda: binding.gqa_attn_decode_layers(q, k, v, o, None, D ** -0.5, ws_l, max_kv_len=S, stream=stream)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        ts = []
+        for _ in range(iters):
+            with torch.cuda.stream(stream):
+                flush_l2(flush)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / NL)
+        return statistics.median(ts)
+    us_seq, us_one = timed(seq), timed(one)
+    nbytes = metrics.decode_bytes(HQ, HKV, D, [S], 4)
+    del q, k, v, o, views
+    torch.cuda.empty_cache()
+    return {"S": S, "layers": NL, "per_layer_calls_us": round(us_seq, 3), "one_launch_us_per_layer": round(us_one, 3),
+            "one_launch_GBps": round(nbytes / us_one / 1e3, 1)}
+
+
 def q4_residual_point(binding, S, device, stream, flush, iters=10, window=100, R_cap=128):
     """q4 decode (Hq=32, Hkv=8, D=128, B=4, 36 layers) with `window` further
     tokens in a bf16 residual window: S quantized keys + the window."""
@@ -842,6 +883,8 @@ def main():
         line["quantize_q4_qwen3_4b"] = quantize_point(binding, device, stream, flush)
         line["q4_residual_decode_qwen3_4b_B4_36_layers"] = [q4_residual_point(binding, S, device, stream, flush)
                                                             for S in (2048, 16384)]
+        line["cross_layer_decode_qwen7b_f32_28_layers"] = [layers_point(binding, S, device, stream, flush)
+                                                           for S in (128, 2048, 32768)]
         pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
         pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
         line["prefill_causal_qwen05b_bf16"] = pf

@@ -39,6 +39,8 @@ EXPORTED = (
     "gqa_attn_decode",
     "gqa_attn_decode_noalloc",
     "gqa_attn_decode_paged",
+    "gqa_attn_decode_layers_workspace_size",
+    "gqa_attn_decode_layers",
     "gqa_attn_quantize_q4",
     "gqa_attn_decode_q4_residual_workspace_size",
     "gqa_attn_decode_q4_residual",
@@ -82,6 +84,11 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                         i32, f32, i32, vp, sz, vp]
     L.gqa_attn_decode_paged.restype = i32
+    L.gqa_attn_decode_layers_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.gqa_attn_decode_layers_workspace_size.restype = sz
+    L.gqa_attn_decode_layers.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp,
+                                         sz, vp]
+    L.gqa_attn_decode_layers.restype = i32
     i64 = ctypes.c_int64
     L.gqa_attn_quantize_q4.argtypes = [vp, i64, vp, vp, vp, i64, i64, i32, i32, i32, i32, vp]
     L.gqa_attn_quantize_q4.restype = i32
@@ -211,6 +218,25 @@ def gqa_attn_quantize_q4(src, codes, scale, bias, dst_row0=0, rows=None, group_s
     rc = lib().gqa_attn_quantize_q4(_ptr(src), S_src, _ptr(codes), _ptr(scale), _ptr(bias), codes.shape[2],
                                     int(dst_row0), B * Hkv, rows, D, int(group_size), _stream(stream))
     _check(rc, "gqa_attn_quantize_q4")
+
+
+def gqa_attn_decode_layers_workspace_size(n_layers, B, Hq, Hkv, D, max_kv_len, dtype) -> int:
+    return lib().gqa_attn_decode_layers_workspace_size(n_layers, B, Hq, Hkv, D, max_kv_len, dtype)
+
+
+def gqa_attn_decode_layers(q, k, v, o, kv_lens, scale, workspace, max_kv_len=None, stream=None):
+    """Layers stacked on a leading axis: q, o [NL,B,Hq,1,D]; k, v [NL,B,Hkv,S_cap,D];
+    kv_lens int32 [B] shared by the layers, or None."""
+    NL, B, Hq, Tq, D = q.shape
+    Hkv, S_cap = k.shape[2], k.shape[3]
+    if Tq != 1:
+        raise ValueError("decode takes one query row per request")
+    if max_kv_len is None:
+        max_kv_len = S_cap
+    rc = lib().gqa_attn_decode_layers(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(kv_lens), NL, B, Hq, Hkv, D,
+                                      S_cap, int(max_kv_len), float(scale), _dtype_code(q), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gqa_attn_decode_layers")
 
 
 def gqa_attn_decode_q4_residual_workspace_size(B, Hq, Hkv, D, max_quant) -> int:

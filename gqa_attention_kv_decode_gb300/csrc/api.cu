@@ -186,6 +186,61 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
   return GQA_OK;
 }
 
+GQA_ATTN_API size_t gqa_attn_decode_layers_workspace_size(int n_layers, int B, int Hq, int Hkv, int D,
+                                                          int max_kv_len, int dtype) {
+  if (n_layers < 1 || long(n_layers) * B > 65535) return 0;
+  if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return 0;
+  const SplitPlan p = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
+                                  decode_ctas_per_sm(dtype));
+  return workspace_layout(n_layers * B, Hq, Hkv, p.n_hc, p.n_split, D).total;
+}
+
+GQA_ATTN_API int gqa_attn_decode_layers(const void* q, const void* k, const void* v, void* o,
+                                        const int32_t* kv_lens, int n_layers, int B, int Hq, int Hkv,
+                                        int D, int S_cap, int max_kv_len, float scale, int dtype,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+  if (n_layers < 1 || long(n_layers) * B > 65535) return GQA_ERR_INVALID_ARG;
+  int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_kv_len, scale);
+  if (rc != GQA_OK) return rc;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  rc = check_ptrs({q, k, v, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  if (kv_lens != nullptr) {
+    rc = check_ptrs({kv_lens}, dev, 4);
+    if (rc != GQA_OK) return rc;
+  }
+  if (workspace == nullptr) return GQA_ERR_WORKSPACE;
+  rc = check_ptrs({workspace}, dev, 256);
+  if (rc == GQA_ERR_INVALID_ARG) return GQA_ERR_WORKSPACE;
+  if (rc != GQA_OK) return rc;
+  DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.kv_lens = kv_lens;
+  a.B = n_layers * B;  // layer l, request b is batch index l * B + b of every stacked tensor
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S_cap = S_cap;
+  a.max_kv_len = max_kv_len;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.workspace = workspace;
+  a.kv_period = B;
+  // the single-layer plan: every (layer, request, head, split) CTA does the
+  // work it does in a one-layer call, so the results are bit-identical
+  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
+                       decode_ctas_per_sm(dtype));
+  if (ws_bytes < workspace_layout(a.B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total) return GQA_ERR_WORKSPACE;
+  if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
 GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const void* v_new,
                                        void* k_pool, void* v_pool, const int32_t* block_table,
                                        const int32_t* kv_lens, void* o, int B, int Hq, int Hkv,

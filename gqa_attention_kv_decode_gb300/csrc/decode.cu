@@ -57,6 +57,7 @@ struct DecodeParams {
   int block_size, max_blocks, num_blocks;
   const void* k_new;  // [B][Hkv][D]: token appended at row kv_lens[b] - 1, or null
   const void* v_new;
+  int kv_period;  // > 0: layers stacked along the batch axis share kv_lens[b % kv_period]
 };
 
 
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   }
   grid_dependency_wait();
 
-  int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
+  int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;
   if (L < 0 || L > p.max_kv_len) {
     if (split == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, GQA_DEV_KVLEN_CLAMPED);
     L = L < 0 ? 0 : p.max_kv_len;
@@ -601,6 +602,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.num_blocks = a.num_blocks;
   p.k_new = a.k_new;
   p.v_new = a.v_new;
+  p.kv_period = a.kv_period;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   cudaError_t e;
   if (a.dtype != GQA_F32)
@@ -619,6 +621,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   m.n_split = p.n_split;
   m.ml = p.ml;
   m.part_o = p.part_o;
+  m.kv_period = a.kv_period;
   const int rows = a.B * a.Hq;
   if (a.dtype == GQA_F32)
     return a.D == 128 ? launch_merge<float, 128>(m, rows, stream) : launch_merge<float, 64>(m, rows, stream);

@@ -63,6 +63,7 @@ struct MmaParams {
   int max_sub, slot_chunk;
   int n_slots;        // partial slots per (request, head) row
   int force_partial;  // write a partial even for a one-split request
+  int kv_period;      // > 0: layers stacked along the batch axis share kv_lens[b % kv_period]
 };
 
 template <int D, int NSTAGE>
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
   }
   grid_dependency_wait();
 
-  int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
+  int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;
   int slot0 = 0;
   if (p.len_sub != nullptr) {
     const int nq = p.len_sub[b];
@@ -513,6 +514,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.slot_chunk = a.slot_chunk > 0 ? a.slot_chunk : 1;
   p.n_slots = a.n_slots > 0 ? a.n_slots : a.plan.n_split;
   p.force_partial = a.force_partial;
+  p.kv_period = a.kv_period;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   if (paged)
     return a.D == 128 ? launch_mma<128, 3, true>(tk, tv, p, grid, stream) : launch_mma<64, 6, true>(tk, tv, p, grid, stream);

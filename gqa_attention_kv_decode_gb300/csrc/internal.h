@@ -67,6 +67,9 @@ struct DecodeArgs {
   // launch_decode_mma_residual
   const int32_t* len_sub = nullptr;
   int max_sub = 0, slot_chunk = 0, n_slots = 0, force_partial = 0;
+  // layers stacked along the batch axis (kv_period = requests per layer):
+  // request b reads kv_lens[b % kv_period]
+  int kv_period = 0;
 };
 
 // Tile height (rows) of the decode kernel for this dtype / head size, and how

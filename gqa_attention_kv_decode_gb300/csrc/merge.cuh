@@ -36,6 +36,7 @@ struct MergeParams {
   const int32_t* n_quant = nullptr;
   int max_quant = 0, res_cap = 0;
   uint32_t* status = nullptr;
+  int kv_period = 0;  // > 0: layers stacked along the batch axis share kv_lens[b % kv_period]
 };
 
 // Merges the split partials of one (request, query head) row, after the split
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
   const int c4 = tid % D4, sg = tid / D4;
   grid_launch_dependents();  // the next call's split kernel may start staging
   grid_dependency_wait();
-  int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
+  int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;
   int n_used;
   if (p.n_quant != nullptr) {
     L = L < 0 ? 0 : L;

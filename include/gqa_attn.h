@@ -108,6 +108,31 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Single-token decode of n_layers layers in one launch (a microbenchmark).
+ *
+ * "Batching Decode Attention Across Requests Got Us 3.83x Real Throughput --
+ * Across Layers Got Us Nothing", results 1 and 2: adding an outermost layer
+ * axis to the decode grid replaces 28-80 launches by one and wins at the
+ * kernel level, but a real decoder cannot use it, because layer l+1's query
+ * needs layer l's complete output.  It is kept for measuring the per-launch
+ * cost, not for model decoding.
+ *
+ * The caller stacks the layers along a leading axis:
+ *   q, o  [n_layers, B, Hq, 1, D]     k, v  [n_layers, B, Hkv, S_cap, D]
+ * (i.e. the gqa_attn_decode layouts with batch n_layers * B); kv_lens [B]
+ * (or NULL) is shared by all layers.  The result equals, bit for bit, n_layers
+ * gqa_attn_decode calls on the per-layer slices: every layer uses the split
+ * plan of a one-layer call.  Workspace: gqa_attn_decode_layers_workspace_size.
+ * n_layers * B <= 65535.  Other arguments and errors as for gqa_attn_decode.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API size_t gqa_attn_decode_layers_workspace_size(int n_layers, int B, int Hq, int Hkv, int D,
+                                                          int max_kv_len, int dtype);
+GQA_ATTN_API int gqa_attn_decode_layers(const void* q, const void* k, const void* v, void* o,
+                                        const int32_t* kv_lens, int n_layers, int B, int Hq, int Hkv,
+                                        int D, int S_cap, int max_kv_len, float scale, int dtype,
+                                        void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Single-token decode over a PAGED KV cache, with an optional fused append of
  * the new token.
  *
