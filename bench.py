@@ -323,6 +323,43 @@ def paged_point(binding, B, device, stream, flush, iters=10, block_size=64):
             "GBps": round(nbytes / us / 1e3, 1)}
 
 
+def varlen_prefill_point(binding, B, device, stream, flush, bf16_peak, iters=20, chunk=512):
+    """Serving-style chunked prefill of B requests at once (Hq=14, Hkv=2,
+    D=64, bf16, causal): request b prefills a chunk of `chunk` queries at the
+    end of its kv_lens[b] keys, kv_lens uniform in [chunk, 8192] (seeded)."""
+    kv_lens = inputs.ragged_kv_lens(B, chunk, 8192, seed=inputs.BASE_SEED + 7 * B)
+    S = int(kv_lens.max())
+    q = inputs.randn((B, 14, chunk, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+    k = inputs.randn((B, 2, S, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+    v = inputs.randn((B, 2, S, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+    o = torch.empty_like(q)
+    ql = torch.full((B,), chunk, dtype=torch.int32, device=device)
+    kl = torch.from_numpy(kv_lens).to(device)
+    torch.cuda.synchronize()
+    launch = lambda: binding.gqa_attn_prefill_varlen(q, k, v, o, ql, kl, 0.125, True, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            launch()
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            flush_l2(flush)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+    flops = sum(metrics.prefill_flops(14, 64, chunk, int(L), causal=True) for L in kv_lens)
+    tf = flops / us / 1e6
+    del q, k, v, o
+    torch.cuda.empty_cache()
+    return {"requests": B, "chunk": chunk, "us": round(us, 2), "TFLOPs": round(tf, 1),
+            "tokens_per_s": round(B * chunk / us * 1e6, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
+
+
 def layers_point(binding, S, device, stream, flush, iters=10, NL=28):
     """Qwen2.5-7B head geometry, fp32, B=1: NL layers as NL gqa_attn_decode
     calls versus one gqa_attn_decode_layers launch over the stacked layers
@@ -885,6 +922,8 @@ def main():
                                                             for S in (2048, 16384)]
         line["cross_layer_decode_qwen7b_f32_28_layers"] = [layers_point(binding, S, device, stream, flush)
                                                            for S in (128, 2048, 32768)]
+        line["varlen_prefill_qwen05b_chunks_512"] = [varlen_prefill_point(binding, B, device, stream, flush, bf16_peak)
+                                                     for B in (4, 16)]
         pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
         pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
         line["prefill_causal_qwen05b_bf16"] = pf

@@ -47,6 +47,7 @@ EXPORTED = (
     "gqa_attn_decode_q4_workspace_size",
     "gqa_attn_decode_q4",
     "gqa_attn_prefill",
+    "gqa_attn_prefill_varlen",
     "gqa_attn_status_string",
     "gqa_attn_read_device_status",
     "gqa_attn_clear_device_status",
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode_q4.restype = i32
     L.gqa_attn_prefill.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
     L.gqa_attn_prefill.restype = i32
+    L.gqa_attn_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+    L.gqa_attn_prefill_varlen.restype = i32
     L.gqa_attn_status_string.argtypes = [i32]
     L.gqa_attn_status_string.restype = ctypes.c_char_p
     L.gqa_attn_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -292,6 +295,19 @@ def gqa_attn_prefill(q, k, v, o, kv_len, scale, causal=True, stream=None):
                                 int(kv_len), S_cap, float(scale), 1 if causal else 0,
                                 _dtype_code(q), _stream(stream))
     _check(rc, "gqa_attn_prefill")
+
+
+def gqa_attn_prefill_varlen(q, k, v, o, q_lens, kv_lens, scale, causal=True, stream=None):
+    """q, o [B,Hq,Tq_cap,D]; k, v [B,Hkv,S_cap,D]; q_lens, kv_lens int32 [B]:
+    request b's q_lens[b] queries aligned to the end of its kv_lens[b] keys."""
+    B, Hq, Tq_cap, D = q.shape
+    Hkv, S_cap = k.shape[1], k.shape[2]
+    if q_lens.dtype != torch.int32 or kv_lens.dtype != torch.int32:
+        raise TypeError("q_lens and kv_lens are int32")
+    rc = lib().gqa_attn_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(q_lens), _ptr(kv_lens), B, Hq,
+                                       Hkv, D, Tq_cap, S_cap, float(scale), 1 if causal else 0, _dtype_code(q),
+                                       _stream(stream))
+    _check(rc, "gqa_attn_prefill_varlen")
 
 
 def gqa_attn_status_string(status: int) -> str:

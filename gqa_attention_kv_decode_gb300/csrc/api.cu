@@ -471,6 +471,46 @@ GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, v
   return GQA_OK;
 }
 
+GQA_ATTN_API int gqa_attn_prefill_varlen(const void* q, const void* k, const void* v, void* o,
+                                         const int32_t* q_lens, const int32_t* kv_lens, int B, int Hq,
+                                         int Hkv, int D, int Tq_cap, int S_cap, float scale, int causal,
+                                         int dtype, void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (Tq_cap < 1 || S_cap < 1) return GQA_ERR_INVALID_ARG;
+  if (long(B) * Hq > 0x7fffffffL || (long(Tq_cap) + 255) / 256 > 65535) return GQA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_BF16 || D != 64) return GQA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  int rc = check_ptrs({q, k, v, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  rc = check_ptrs({q_lens, kv_lens}, dev, 4);
+  if (rc != GQA_OK) return rc;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.q_len = Tq_cap;
+  a.kv_len = S_cap;
+  a.S_cap = S_cap;
+  a.scale = scale;
+  a.causal = causal;
+  a.q_lens = q_lens;
+  a.kv_lens = kv_lens;
+  const cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
 GQA_ATTN_API int gqa_attn_read_device_status(const void* workspace, uint32_t* out, void* stream) {
   if (workspace == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
   int dev = 0;

@@ -118,6 +118,10 @@ struct PrefillArgs {
   int B, Hq, Hkv, D, q_len, kv_len, S_cap;
   float scale;
   int causal;
+  // per-request lengths (device int32 [B]) or null; with them q_len is the
+  // rows per head of Q and O and every request may use up to S_cap keys
+  const int32_t* q_lens = nullptr;
+  const int32_t* kv_lens = nullptr;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);

@@ -87,6 +87,12 @@ struct PrefillParams {
   int kv_splits;        // CTAs of a cluster sharing one pair's KV tiles (1, 2, 4 or 8)
   float qk_scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  int q_pitch;          // rows per head of Q and O
+  // per-request lengths (varlen; null: q_len, kv_len for every request):
+  // request b has clamp(kv_lens[b], 0, kv_len) keys and clamp(q_lens[b], 0,
+  // min(q_len, its keys)) queries, aligned to the end of its keys
+  const int32_t* q_lens;
+  const int32_t* kv_lens;
 };
 
 // Bounded wait shared by the whole CTA: once one thread gives up, the
@@ -168,12 +174,20 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int b = bh / p.Hq;
   const int g = h / p.n_rep;
   const int m0 = pair * 2 * BM;
-  const int off = p.kv_len - p.q_len;  // query row i sits at key position off + i
+  int q_len = p.q_len, kv_len = p.kv_len;
+  if (p.q_lens != nullptr) {
+    kv_len = min(max(p.kv_lens[b], 0), p.kv_len);
+    q_len = min(max(p.q_lens[b], 0), min(p.q_len, kv_len));
+    // a pair past this request's queries has nothing to do (the CTAs of a
+    // cluster share the pair, so they leave together)
+    if (m0 >= q_len) return;
+  }
+  const int off = kv_len - q_len;  // query row i sits at key position off + i
 
   auto nkv_for = [&](int mstart) -> int {
-    if (mstart >= p.q_len) return 0;
-    int n = (p.kv_len + BN - 1) / BN;
-    if (p.causal) n = min(n, (off + min(mstart + BM - 1, p.q_len - 1)) / BN + 1);
+    if (mstart >= q_len) return 0;
+    int n = (kv_len + BN - 1) / BN;
+    if (p.causal) n = min(n, (off + min(mstart + BM - 1, q_len - 1)) / BN + 1);
     return n;
   };
   // The pair's KV tiles [0, nkv_all) are cut into ks contiguous shares; this
@@ -268,12 +282,24 @@ __global__ void __launch_bounds__(NTHR, 1)
       constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;
       constexpr uint64_t V_KSTEP = 2048 >> 4;  // 16 keys of the MN-major V tile
       const uint32_t d = tmem + TM_O + t * 64, a = tmem + TM_P + t * 64;
+      // Per-request lengths: the V map spans the whole cache, so the last KV
+      // tile may hold rows past kv_len (anything, NaN included; their P is 0
+      // but 0 * NaN is NaN).  Both P.V warps zero those rows first.
+      const int j_zero = (p.q_lens != nullptr && kv_len % BN != 0) ? (kv_len - 1) / BN - j_lo : -1;
       for (int j = 0; j < nkv_max; ++j) {
         const int st = j % NST;
         // Waited for even past this tile's last KV tile: the load of tile j
         // orders this warp's arrival on B_KE[st] after the previous phase,
         // so one warp can never arrive twice within a phase.
         cta_wait(&bars[B_VF + st], uint32_t(j / NST) & 1u, abort_flag, p.wait_limit_ns);
+        if (j == j_zero) {
+          unsigned char* vt = smem + OFF_V + st * TILE_BYTES;
+          const int r0 = kv_len % BN;  // first row to clear (rows are 128 bytes; swizzle stays inside a row)
+          for (int i = (warp - 10) * 32 + lane; i < (BN - r0) * 8; i += 64)
+            *reinterpret_cast<uint4*>(vt + (r0 + i / 8) * 128 + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+          asm volatile("bar.sync 1, 64;" ::: "memory");  // both P.V warps are done clearing
+        }
         if (j < nkv) {
           const uint64_t vd = vdesc + st * TILE_STEP;
 #pragma unroll
@@ -304,7 +330,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t tO = tmem + TM_O + t * 64 + lane_off;
     const uint32_t tP = tmem + TM_P + t * 64 + lane_off;
     const int qi = m0 + t * BM + (tid & (BM - 1));
-    const int last_key = p.causal ? min(off + qi, p.kv_len - 1) : p.kv_len - 1;
+    const int last_key = p.causal ? min(off + qi, kv_len - 1) : kv_len - 1;
     const float c = p.qk_scale_log2;  // > 0 (the scale is checked on the host)
     float m_ref = -INFINITY, lsum = 0.f;
     for (int j = 0; j < nkv; ++j) {
@@ -390,14 +416,14 @@ __global__ void __launch_bounds__(NTHR, 1)
     // ---- epilogue: O / l, bf16, to global memory ----
     if (!SPLIT) {
       if (nkv > 0) {
-        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD;
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
         const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {  // 32 columns at a time keeps the register count down
           uint32_t o[32];
           tmem_ld32(tO + cc * 32, o);
           tmem_wait_ld();
-          if (qi < p.q_len) {
+          if (qi < q_len) {
 #pragma unroll
             for (int e8 = 0; e8 < 4; ++e8) {
               uint32_t w[4];
@@ -442,8 +468,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         dsmem_st4(ra + 64 * 4, make_float4(m_ref, lsum, 0.f, 0.f));
       }
       cluster_sync_all();  // every partial has arrived
-      if (warp % ks == rank && qi < p.q_len) {
-        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_len + qi) * HD;
+      if (warp % ks == rank && qi < q_len) {
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
         const int slot = warp / ks;
         float M = -INFINITY;
         for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 64]);
@@ -497,9 +523,14 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_pi
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (a.D != HD) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, a.q, a.q_len, a.q_len, uint64_t(a.B) * a.Hq) ||
-      !make_map(&tk, a.k, a.kv_len, a.S_cap, uint64_t(a.B) * a.Hkv) ||
-      !make_map(&tv, a.v, a.kv_len, a.S_cap, uint64_t(a.B) * a.Hkv))
+  // uniform lengths: the K/V maps end at kv_len, so rows past it arrive as
+  // zeros; per-request lengths: the maps span the whole buffers and the
+  // kernel masks and clears what lies past each request's lengths
+  const bool varlen = a.q_lens != nullptr;
+  const uint64_t q_rows = a.q_len, kv_rows = varlen ? uint64_t(a.S_cap) : uint64_t(a.kv_len);
+  if (!make_map(&tq, a.q, q_rows, a.q_len, uint64_t(a.B) * a.Hq) ||
+      !make_map(&tk, a.k, kv_rows, a.S_cap, uint64_t(a.B) * a.Hkv) ||
+      !make_map(&tv, a.v, kv_rows, a.S_cap, uint64_t(a.B) * a.Hkv))
     return cudaErrorInvalidValue;
   PrefillParams p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -507,7 +538,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.Hkv = a.Hkv;
   p.n_rep = a.Hq / a.Hkv;
   p.q_len = a.q_len;
-  p.kv_len = a.kv_len;
+  p.kv_len = varlen ? a.S_cap : a.kv_len;
+  p.q_pitch = a.q_len;
+  p.q_lens = a.q_lens;
+  p.kv_lens = a.kv_lens;
   p.n_pairs = (a.q_len + 2 * BM - 1) / (2 * BM);
   p.causal = a.causal;
   p.qk_scale_log2 = float(double(a.scale) * 1.4426950408889634);

@@ -175,6 +175,31 @@ GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const v
                                        size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Prefill of a batch of requests with their own lengths (varlen, chunked).
+ *
+ * Serving mixes prefill chunks of many requests, each at its own position in
+ * its own cache; gqa_attn_prefill takes one (q_len, kv_len) for the whole
+ * batch.  Here request b has q_lens[b] queries aligned to the end of its
+ * kv_lens[b] keys ("Fused attention makes a 4,096-token Qwen2 prefill on
+ * Metal 4.5x faster", "Cause and workaround", item 2: with the causal mask a
+ * chunk at an offset sees all earlier keys).
+ *
+ *   q, o      bf16 [B, Hq, Tq_cap, D]   rows [0, q_lens[b]) of request b
+ *                                       (other rows of o are not written)
+ *   k, v      bf16 [B, Hkv, S_cap, D]   rows [0, kv_lens[b]) of request b;
+ *                                       rows past it may hold anything
+ *   q_lens,   device int32 [B]; kv_lens[b] is clamped into [0, S_cap] and
+ *   kv_lens   q_lens[b] into [0, min(Tq_cap, kv_lens[b])]
+ *   causal    1: query i of request b sees keys j <= i + kv_lens[b] - q_lens[b];
+ *             0: all kv_lens[b] keys
+ * D = 64 (bf16).  Other errors as for gqa_attn_prefill.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API int gqa_attn_prefill_varlen(const void* q, const void* k, const void* v, void* o,
+                                         const int32_t* q_lens, const int32_t* kv_lens, int B, int Hq,
+                                         int Hkv, int D, int Tq_cap, int S_cap, float scale, int causal,
+                                         int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Decode over a 4-bit cache followed by an unquantized residual window.
  *
  * "Batching Decode Attention Across Requests ...", VeloxQuant-MLX blog,
