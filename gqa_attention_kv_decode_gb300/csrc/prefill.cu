@@ -336,11 +336,13 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int j = 0; j < nkv; ++j) {
       cta_wait(&bars[B_S + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
+      // the row's 128 scores, with the maximum of each 32 from the load itself
       uint32_t s[BN];
-      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(s));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+      float rmx[4];
+      tmem_ld32_max(tS, *reinterpret_cast<uint32_t(*)[32]>(s), rmx[0]);
+      tmem_ld32_max(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32), rmx[1]);
+      tmem_ld32_max(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64), rmx[2]);
+      tmem_ld32_max(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96), rmx[3]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -348,19 +350,22 @@ __global__ void __launch_bounds__(NTHR, 1)
 
       const int n0 = (j_lo + j) * BN;
       if (__any_sync(0xffffffffu, n0 + BN - 1 > last_key)) {  // the diagonal (or the end) crosses this tile
+        // mask, then take the maximum again over what is left
 #pragma unroll
         for (int e = 0; e < BN; ++e)
           if (n0 + e > last_key) s[e] = 0xff800000u;  // -inf
-      }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < BN; e += 8) {
-        mx[0] = max3f(mx[0], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
-        mx[1] = max3f(mx[1], __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]));
-        mx[2] = max3f(mx[2], __uint_as_float(s[e + 4]), __uint_as_float(s[e + 5]));
-        mx[3] = max3f(mx[3], __uint_as_float(s[e + 6]), __uint_as_float(s[e + 7]));
+        for (int e = 0; e < BN; e += 8) {
+          mx[0] = max3f(mx[0], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+          mx[1] = max3f(mx[1], __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]));
+          mx[2] = max3f(mx[2], __uint_as_float(s[e + 4]), __uint_as_float(s[e + 5]));
+          mx[3] = max3f(mx[3], __uint_as_float(s[e + 6]), __uint_as_float(s[e + 7]));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rmx[i] = mx[i];
       }
-      const float tmax = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
+      const float tmax = max3f(rmx[0], rmx[1], fmaxf(rmx[2], rmx[3])) * c;
       if (j == 0) {
         // The first tile of the share.  Without a split it holds key 0, which
         // every row sees; with one, a row may see no key of the share at all
