@@ -16,10 +16,11 @@
 //
 // A lane loads 16 bytes (8 elements); D/8 lanes hold a row and 8 lanes a
 // group, whose minimum and maximum come from three xor shuffles.  A warp keeps
-// UNR such loads in flight (4 rows at D = 128) before it computes.  Codes are
+// UNR = 4 such loads in flight (8 rows at D = 128) before it computes.  Codes are
 // written as 4 bytes per lane (one contiguous D/2-byte run per row), the
 // group's scale and bias by its first lane.  HBM-bound: 2D bytes read,
-// D/2 + 4 D/64 written per row.
+// D/2 + 4 D/64 written per row.  The grid is (row blocks, heads), so no lane
+// divides to find its head.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,59 +41,69 @@ struct QuantParams {
 };
 
 template <int D>
+struct QuantCfg {
+  static constexpr int LPR = D / 8;     // lanes per row (8 elements a lane)
+  static constexpr int RPL = 32 / LPR;  // rows per warp-wide load
+  static constexpr int UNR = 4;         // loads in flight per lane
+  static constexpr int ROWS_PER_CTA = 8 * RPL * UNR;  // 8 warps
+};
+
+template <int D>
 __global__ void __launch_bounds__(256) quantize_q4_kernel(const QuantParams p) {
-  constexpr int LPR = D / 8;          // lanes per row (8 elements a lane)
-  constexpr int RPL = 32 / LPR;       // rows per warp-wide load
-  constexpr int UNR = 2;              // loads in flight per lane
+  constexpr int LPR = QuantCfg<D>::LPR;
+  constexpr int RPL = QuantCfg<D>::RPL;
+  constexpr int UNR = QuantCfg<D>::UNR;
   constexpr int NG = D / 64;          // groups per row
   const int lane = threadIdx.x & 31;
-  const long long total = p.heads * p.rows;
-  const long long row0 = ((long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * (RPL * UNR);
+  const long long head = blockIdx.y + (long long)gridDim.y * blockIdx.z;
+  if (head >= p.heads) return;
+  const int row0 = (int(blockIdx.x) * 8 + (int(threadIdx.x) >> 5)) * (RPL * UNR);
   const int col = lane % LPR;         // 8-element chunk of the row
+  const __nv_bfloat16* src = p.src + head * p.src_head_rows * D + col * 8;
+  const long long dst0 = head * p.dst_head_rows + p.dst_row0;
   uint4 w[UNR];
-  long long rows[UNR];
+  int rows[UNR];
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
     rows[u] = row0 + u * RPL + lane / LPR;
-    if (rows[u] < total) {
-      const long long head = rows[u] / p.rows, r = rows[u] % p.rows;
-      w[u] = *reinterpret_cast<const uint4*>(p.src + (head * p.src_head_rows + r) * D + col * 8);
-    } else {
-      w[u] = make_uint4(0u, 0u, 0u, 0u);
-    }
+    w[u] = rows[u] < p.rows ? *reinterpret_cast<const uint4*>(src + (long long)rows[u] * D)
+                            : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
-    float x[8];
     const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+    // group minimum and maximum on the bf16 pairs (exact), carried through the
+    // shuffles as one (min, -max) pair
+    __nv_bfloat162 bw[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = bf16x2_to_float2(ww[i]);
-      x[2 * i] = f.x;
-      x[2 * i + 1] = f.y;
-    }
-    float lo = fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
-    float hi = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+    for (int i = 0; i < 4; ++i) bw[i] = *reinterpret_cast<const __nv_bfloat162*>(&ww[i]);
+    const __nv_bfloat162 mn = __hmin2(__hmin2(bw[0], bw[1]), __hmin2(bw[2], bw[3]));
+    const __nv_bfloat162 nmx = __hneg2(__hmax2(__hmax2(bw[0], bw[1]), __hmax2(bw[2], bw[3])));
+    __nv_bfloat162 v = __hmin2(__lows2bfloat162(mn, nmx), __highs2bfloat162(mn, nmx));  // (lo, -hi)
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1) {  // the 8 lanes of a group
-      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, m));
-      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, m));
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<const uint32_t*>(&v), m);
+      v = __hmin2(v, *reinterpret_cast<const __nv_bfloat162*>(&o));
     }
-    if (rows[u] >= total) continue;
+    if (rows[u] >= p.rows) continue;
+    const float lo = __bfloat162float(__low2bfloat16(v)), hi = -__bfloat162float(__high2bfloat16(v));
     const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.f));
     const __half b16 = __float2half_rn(lo);
     const float s = __half2float(s16), bb = __half2float(b16);
     const float rcp = __frcp_rn(s);
+    // per pair: (x - bias) * r (x + (-bias) is x - bias), rounded to the
+    // nearest integer, ties to even, by the saturating conversion (negative
+    // values and NaN give 0), then capped at 15
+    const float2 nb = make_float2(-bb, -bb), r2 = make_float2(rcp, rcp);
     uint32_t packed = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      // clamping to [0, 15] before rounding gives the same codes as after it
-      const float t = fminf(fmaxf(__fmul_rn(__fsub_rn(x[i], bb), rcp), 0.f), 15.f);
-      const uint32_t q = __float2uint_rn(t);
-      packed |= (s > 0.f ? q : 0u) << (4 * i);
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __fmul2_rn(__fadd2_rn(bf16x2_to_float2(ww[i]), nb), r2);
+      const uint32_t k0 = min(__float2uint_rn(t.x), 15u), k1 = min(__float2uint_rn(t.y), 15u);
+      packed += (k0 + 16u * k1) << (8 * i);
     }
-    const long long head = rows[u] / p.rows, r = rows[u] % p.rows;
-    const long long drow = head * p.dst_head_rows + p.dst_row0 + r;
+    if (!(s > 0.f)) packed = 0u;
+    const long long drow = dst0 + rows[u];
     *reinterpret_cast<uint32_t*>(p.codes + drow * (D / 2) + col * 4) = packed;
     if ((col & 7) == 0) {
       p.scale[drow * NG + col / 8] = s16;
@@ -112,9 +123,8 @@ extern "C" GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_he
                                                  int group_size, void* stream) {
   if (heads < 1 || rows < 1 || (D != 64 && D != 128) || group_size != 64) return GQA_ERR_INVALID_ARG;
   if (rows > src_head_rows || dst_row0 < 0 || dst_row0 + rows > dst_head_rows) return GQA_ERR_INVALID_ARG;
-  const long long total = (long long)heads * rows;
-  const long long rows_per_cta = 8LL * (D == 128 ? 4 : 8);  // 8 warps x (rows per load x loads in flight)
-  if ((total + rows_per_cta - 1) / rows_per_cta > 0x7fffffffLL) return GQA_ERR_INVALID_ARG;
+  const int rows_per_cta = D == 128 ? QuantCfg<128>::ROWS_PER_CTA : QuantCfg<64>::ROWS_PER_CTA;
+  if (heads > 65535LL * 65535LL) return GQA_ERR_INVALID_ARG;
   if (src == nullptr || codes == nullptr || scale == nullptr || bias == nullptr) return GQA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(src) % 16) != 0 || (reinterpret_cast<uintptr_t>(codes) % 4) != 0 ||
       (reinterpret_cast<uintptr_t>(scale) % 2) != 0 || (reinterpret_cast<uintptr_t>(bias) % 2) != 0)
@@ -141,7 +151,9 @@ extern "C" GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_he
   p.dst_row0 = dst_row0;
   p.heads = heads;
   p.rows = rows;
-  const unsigned grid = unsigned((total + rows_per_cta - 1) / rows_per_cta);
+  // (row blocks of a head, heads): heads spill from y into z past 65535
+  const dim3 grid(unsigned((rows + rows_per_cta - 1) / rows_per_cta), unsigned(heads < 65535 ? heads : 65535),
+                  unsigned((heads + 65534) / 65535));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 128)
     quantize_q4_kernel<128><<<grid, 256, 0, s>>>(p);
