@@ -59,6 +59,13 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def replica_value(world: int, step_units: float, ms_per_step: float) -> float:
+    """Whole-job rate in units/s / 1e9 (GB/s for bytes): every one of the
+    `world` replicas processes `step_units` per step, and the step time is the
+    maximum over ranks."""
+    return world * step_units / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -835,7 +842,7 @@ def main():
     n_split = binding.gqa_attn_decode_num_splits(1, HQ, HKV, D, S, binding.GQA_F32)
     launches_per_call = 2 if n_split > 1 else 1  # split kernel (+ merge kernel)
     achieved = per_launch_bytes / avg_launch_us / 1e3
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = replica_value(world, step_bytes, ms_per_step)
 
     # end to end through the public API with host buffers
     e2e_steps = 3
@@ -867,7 +874,7 @@ def main():
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_value = replica_value(world, step_bytes, e2e_ms)
     del host, host_out
 
     traffic = recorded_traffic("decode.cu", "decode_f32_d128_nrep7_S32768")
