@@ -330,23 +330,32 @@ def paged_point(binding, B, device, stream, flush, iters=10, block_size=64):
             "GBps": round(nbytes / us / 1e3, 1)}
 
 
-def varlen_prefill_point(binding, B, device, stream, flush, bf16_peak, iters=20, chunk=512):
+PREFILL_LAYERS = 24  # Qwen2.5-0.5B: one prefill step is this many layer launches
+
+
+def varlen_prefill_point(binding, B, device, stream, flush, bf16_peak, iters=8, chunk=512, NL=PREFILL_LAYERS):
     """Serving-style chunked prefill of B requests at once (Hq=14, Hkv=2,
     D=64, bf16, causal): request b prefills a chunk of `chunk` queries at the
-    end of its kv_lens[b] keys, kv_lens uniform in [chunk, 8192] (seeded)."""
+    end of its kv_lens[b] keys, kv_lens uniform in [chunk, 8192] (seeded).
+    Timed like prefill_point: NL launches on distinct buffers per step."""
     kv_lens = inputs.ragged_kv_lens(B, chunk, 8192, seed=inputs.BASE_SEED + 7 * B)
     S = int(kv_lens.max())
-    q = inputs.randn((B, 14, chunk, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
-    k = inputs.randn((B, 2, S, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
-    v = inputs.randn((B, 2, S, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
-    o = torch.empty_like(q)
+    layers = []
+    for l in range(NL):
+        q = inputs.randn((B, 14, chunk, 64), inputs.tensor_seed(l, 0), torch.bfloat16, device)
+        k = inputs.randn((B, 2, S, 64), inputs.tensor_seed(l, 1), torch.bfloat16, device)
+        v = inputs.randn((B, 2, S, 64), inputs.tensor_seed(l, 2), torch.bfloat16, device)
+        layers.append((q, k, v, torch.empty_like(q)))
     ql = torch.full((B,), chunk, dtype=torch.int32, device=device)
     kl = torch.from_numpy(kv_lens).to(device)
     torch.cuda.synchronize()
-    launch = lambda: binding.gqa_attn_prefill_varlen(q, k, v, o, ql, kl, 0.125, True, stream)
+
+    def step():
+        for q, k, v, o in layers:
+            binding.gqa_attn_prefill_varlen(q, k, v, o, ql, kl, 0.125, True, stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
-            launch()
+            step()
     evs = []
     with torch.cuda.stream(stream):
         for _ in range(iters):
@@ -354,16 +363,16 @@ def varlen_prefill_point(binding, B, device, stream, flush, bf16_peak, iters=20,
             e1 = torch.cuda.Event(enable_timing=True)
             flush_l2(flush)
             e0.record(stream)
-            launch()
+            step()
             e1.record(stream)
             evs.append((e0, e1))
     torch.cuda.synchronize()
-    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs) / NL
     flops = sum(metrics.prefill_flops(14, 64, chunk, int(L), causal=True) for L in kv_lens)
     tf = flops / us / 1e6
-    del q, k, v, o
+    del layers
     torch.cuda.empty_cache()
-    return {"requests": B, "chunk": chunk, "us": round(us, 2), "TFLOPs": round(tf, 1),
+    return {"requests": B, "chunk": chunk, "layers": NL, "us": round(us, 2), "TFLOPs": round(tf, 1),
             "tokens_per_s": round(B * chunk / us * 1e6, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
 
 
@@ -530,20 +539,28 @@ def q4_point(binding, S, device, stream, flush, iters=10):
     return {"S": S, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
 
 
-def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iters=20):
+def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iters=8, NL=PREFILL_LAYERS):
     """Hq=14, Hkv=2, D=64, bf16, causal, queries aligned to the end of the keys.
 
-    Each timed launch follows an L2 flush on the same stream; the flush keeps
-    the device busy while the host enqueues the launch, so the events bracket
-    the kernel and not the host's launch overhead."""
-    q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
-    k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
-    v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
-    o = torch.empty_like(q)
+    One step is NL launches on NL distinct buffer sets (a prefill through the
+    model's layers), timed with one event pair after an L2 flush: no launch
+    finds its inputs in L2, and launches follow each other as in a model
+    instead of each being bracketed by its own events.  Per-launch time =
+    step time / NL (median over the steps)."""
+    layers = []
+    for l in range(NL):
+        q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(l, 0), torch.bfloat16, device)
+        k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(l, 1), torch.bfloat16, device)
+        v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(l, 2), torch.bfloat16, device)
+        layers.append((q, k, v, torch.empty_like(q)))
     torch.cuda.synchronize()
+
+    def step():
+        for q, k, v, o in layers:
+            binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
-            binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
+            step()
     evs = []
     with torch.cuda.stream(stream):
         for _ in range(iters):
@@ -551,14 +568,16 @@ def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iter
             e1 = torch.cuda.Event(enable_timing=True)
             flush_l2(flush)
             e0.record(stream)
-            binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
+            step()
             e1.record(stream)
             evs.append((e0, e1))
     torch.cuda.synchronize()
-    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs) / NL
     flops = metrics.prefill_flops(14, 64, q_len, kv_len, causal=True)
     tf = flops / us / 1e6
-    return {"q_len": q_len, "kv_len": kv_len, "us": round(us, 2), "TFLOPs": round(tf, 1),
+    del layers
+    torch.cuda.empty_cache()
+    return {"q_len": q_len, "kv_len": kv_len, "layers": NL, "us": round(us, 2), "TFLOPs": round(tf, 1),
             "tokens_per_s": round(q_len / us * 1e6, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
 
 
@@ -938,7 +957,7 @@ def main():
         line["roofline_prefill"] = {"bound": "tensor", "achieved": big["TFLOPs"], "peak": bf16_peak,
                                     "unit": "TFLOP/s", "frac": big["frac_of_bf16_peak"],
                                     "traffic": recorded_traffic("prefill.cu", "prefill_causal_T16384"),
-                                    "kernel": "prefill_kernel (T=16384 causal)",
+                                    "kernel": "prefill_kernel (T=16384 causal, 24 layer launches per step)",
                                     "peak_source": peak_src + " bf16 burst"}
         del flush
     if rank == 0:

@@ -67,10 +67,16 @@ constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 // Split-KV exchange (after the main loop, over the K/V stages): a partial row
-// is (O[64], m, l) padded to 68 floats; a unit is 32 rows of one tile; the 8
-// units of a CTA are spread over the cluster.
-constexpr int XROW = 68, XUNIT = 32 * XROW;
+// is (O[64], m, l) padded to 17 float4 chunks; a unit is 32 rows of one tile,
+// stored chunk-major ([chunk][row][4]) so that the 32 lanes of a warp write
+// one 512-byte run per remote store; the 8 units of a CTA are spread over the
+// cluster.
+constexpr int XCHUNKS = 17, XUNIT = XCHUNKS * 32 * 4;  // floats per unit
 static_assert(8 * XUNIT * 4 <= 2 * NST * TILE_BYTES, "exchange buffer fits in the K/V stages");
+// float offset of chunk c of row `lane` in unit (src, slot) of the exchange
+__device__ __forceinline__ int xidx(int src, int slot, int units_per_rank, int c, int lane) {
+  return (((src * units_per_rank + slot) * XCHUNKS + c) * 32 + lane) * 4;
+}
 
 // mbarrier slots ([t] = per query tile)
 //   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
@@ -452,7 +458,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       cluster_sync_all();  // every CTA of the cluster is done with its stages
       {
         const int dst_rank = warp % ks, slot = warp / ks;
-        const float* loc = xbuf + ((rank * (8 / ks) + slot) * 32 + lane) * XROW;
+        const float* loc = xbuf + xidx(rank, slot, 8 / ks, 0, lane);
         const uint32_t ra = dsmem_addr(loc, uint32_t(dst_rank));
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -466,24 +472,24 @@ __global__ void __launch_bounds__(NTHR, 1)
           }
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4)
-            dsmem_st4(ra + (cc * 8 + e4) * 16,
+            dsmem_st4(ra + (cc * 8 + e4) * 512,
                       make_float4(__uint_as_float(o[4 * e4]), __uint_as_float(o[4 * e4 + 1]),
                                   __uint_as_float(o[4 * e4 + 2]), __uint_as_float(o[4 * e4 + 3])));
         }
-        dsmem_st4(ra + 64 * 4, make_float4(m_ref, lsum, 0.f, 0.f));
+        dsmem_st4(ra + 16 * 512, make_float4(m_ref, lsum, 0.f, 0.f));
       }
       cluster_sync_all();  // every partial has arrived
       if (warp % ks == rank && qi < q_len) {
         __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
         const int slot = warp / ks;
         float M = -INFINITY;
-        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 64]);
+        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[xidx(src, slot, 8 / ks, 16, lane)]);
         float w_src[8], L = 0.f;
 #pragma unroll
         for (int src = 0; src < 8; ++src) {
-          const float ms = src < ks ? xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 64] : -INFINITY;
+          const float ms = src < ks ? xbuf[xidx(src, slot, 8 / ks, 16, lane)] : -INFINITY;
           w_src[src] = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
-          if (src < ks) L += xbuf[((src * (8 / ks) + slot) * 32 + lane) * XROW + 65] * w_src[src];
+          if (src < ks) L += xbuf[xidx(src, slot, 8 / ks, 16, lane) + 1] * w_src[src];
         }
         const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / L;
 #pragma unroll
@@ -492,9 +498,8 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
           for (int src = 0; src < 8; ++src) {
             if (src < ks) {
-              const float* row = xbuf + ((src * (8 / ks) + slot) * 32 + lane) * XROW + e8 * 8;
-              const float4 v0 = *reinterpret_cast<const float4*>(row);
-              const float4 v1 = *reinterpret_cast<const float4*>(row + 4);
+              const float4 v0 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, 8 / ks, 2 * e8, lane));
+              const float4 v1 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, 8 / ks, 2 * e8 + 1, lane));
               const float w = w_src[src];
               acc8[0] += v0.x * w; acc8[1] += v0.y * w; acc8[2] += v0.z * w; acc8[3] += v0.w * w;
               acc8[4] += v1.x * w; acc8[5] += v1.y * w; acc8[6] += v1.z * w; acc8[7] += v1.w * w;
