@@ -143,6 +143,16 @@ __device__ __forceinline__ void set_max_regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Named barriers 2 and 3 alternate the exponentials of the two softmax
+// warpgroups (256 threads each: 128 wait, the other 128 arrive).
+constexpr int BAR_TURN_A = 2, BAR_TURN_B = 3;
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Exponentials of 64 scores s[0..63] of one row against the reference m
 // (P = 2^(s*c - m)), packed as 32 bf16 pairs; their sum is added to acc.
 __device__ __forceinline__ void exp_half(const uint32_t* s, float2 c, float2 mm, uint32_t (&pw)[32],
@@ -339,6 +349,16 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int last_key = p.causal ? min(off + qi, kv_len - 1) : kv_len - 1;
     const float c = p.qk_scale_log2;  // > 0 (the scale is checked on the host)
     float m_ref = -INFINITY, lsum = 0.f;
+    // The two warpgroups share the schedulers, the XU and the FMA pipe; run
+    // together their exponentials take twice as long while their P stores
+    // and waits leave those pipes idle.  For the tiles both have (j < nmin)
+    // they take turns: A computes the exponentials of tile j while B stores
+    // and loads, then B while A does.  The trip counts are fixed per CTA, so
+    // every bar.sync meets exactly 128 arrivals: A syncs on TURN_A nmin times
+    // and B arrives on it nmin times (once before its loop); B syncs on TURN_B
+    // nmin times and A arrives on it nmin times.
+    const int nmin = min(nkv0, nkv1);
+    if (t == 1 && nmin > 0) named_bar_arrive(BAR_TURN_A, 256);
     for (int j = 0; j < nkv; ++j) {
       cta_wait(&bars[B_S + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
       tc_fence_after();
@@ -402,12 +422,24 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
       }
       const float m_use = (SPLIT && m_ref == -INFINITY) ? 0.f : m_ref;
-      const float2 cc2 = make_float2(c, c), mm = make_float2(-m_use, -m_use);
+      float mu = m_use;
+      if (j < nmin) named_bar_sync(t == 0 ? BAR_TURN_A : BAR_TURN_B, 256);  // this warpgroup's turn
+      // the exponentials depend on mu: keep the compiler from starting them
+      // before the turn begins
+      asm volatile("" : "+f"(mu));
+      const float2 cc2 = make_float2(c, c), mm = make_float2(-mu, -mu);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pw[32];
         exp_half(s + half * 64, cc2, mm, pw, acc);
+        // after the last exponentials of the tile (their sums are inputs
+        // here, so none is moved past the hand-over): the other's turn
+        if (half == 1 && j < nmin) {
+          asm volatile("" ::"f"(acc[0].x), "f"(acc[0].y), "f"(acc[1].x), "f"(acc[1].y), "f"(acc[2].x),
+                       "f"(acc[2].y), "f"(acc[3].x), "f"(acc[3].y));
+          if (t == 0 || j < nmin - 1) named_bar_arrive(t == 0 ? BAR_TURN_B : BAR_TURN_A, 256);
+        }
         // P_t half may be overwritten once the previous P.V has read it
         if (j > 0) cta_wait(&bars[(half ? B_O1 : B_O0) + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
         tc_fence_after();
