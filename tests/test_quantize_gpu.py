@@ -109,3 +109,14 @@ def test_quantizer_rejects_bad_ranges():
     with pytest.raises(binding.GqaAttnError) as e:
         binding.gqa_attn_quantize_q4(x, codes, scale, bias, dst_row0=1)  # 1 + 8 rows > 8
     assert e.value.status == binding.GQA_ERR_INVALID_ARG
+
+
+def test_quantizer_more_heads_than_one_grid_row():
+    # 70,001 heads of 3 rows: the launch spreads heads over two grid dimensions
+    # (65,535 per row), so the last heads sit in the second z slice
+    heads, S, D = 70001, 3, 64
+    x = inputs.randn((1, heads, S, D), 97, torch.float32, DEV).to(torch.bfloat16)
+    codes, scale, bias = empty_cache(1, heads, S, D)
+    binding.gqa_attn_quantize_q4(x, codes, scale, bias, dst_row0=0)
+    torch.cuda.synchronize()
+    check_rows(x, codes, scale, bias, 0)
