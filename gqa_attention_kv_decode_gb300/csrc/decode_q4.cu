@@ -395,15 +395,17 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
       const float s = NG == 2 ? s2.x + s2.y : s2.x;
       sv[i] = (FULL || (i < 2 ? kA : kB) < wvalid) ? s : -INFINITY;
     }
+    // lazy reference: raised only when a tile's maximum exceeds it by 2^8.
+    // Whether any column's maximum does is decided from each lane's own
+    // scores; the maxima over the 8 lanes of a column are formed only then.
     float mL = fmaxf(sv[0], sv[2]), mH = fmaxf(sv[1], sv[3]);
+    if (__any_sync(0xffffffffu, mL > m_refL + 8.f || mH > m_refH + 8.f)) {
 #pragma unroll
-    for (int m = 4; m <= 16; m <<= 1) {
-      mL = fmaxf(mL, __shfl_xor_sync(0xffffffffu, mL, m));
-      mH = fmaxf(mH, __shfl_xor_sync(0xffffffffu, mH, m));
-    }
-    // lazy reference: raised only when a tile's maximum exceeds it by 2^8
-    const bool rL = mL > m_refL + 8.f, rH = mH > m_refH + 8.f;
-    if (__any_sync(0xffffffffu, rL || rH)) {
+      for (int m = 4; m <= 16; m <<= 1) {
+        mL = fmaxf(mL, __shfl_xor_sync(0xffffffffu, mL, m));
+        mH = fmaxf(mH, __shfl_xor_sync(0xffffffffu, mH, m));
+      }
+      const bool rL = mL > m_refL + 8.f, rH = mH > m_refH + 8.f;
       const float aL = rL ? fast_exp2(m_refL - mL) : 1.f;
       const float aH = rH ? fast_exp2(m_refH - mH) : 1.f;
       if (rL) m_refL = mL;
