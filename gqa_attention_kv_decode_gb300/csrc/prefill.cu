@@ -190,6 +190,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int b = bh / p.Hq;
   const int g = h / p.n_rep;
   const int m0 = pair * 2 * BM;
+  // Launched with programmatic stream serialisation: the next grid in the
+  // stream may start launching at once (its CTAs wait in the same way), and
+  // nothing the previous grid writes is read or written before it is done.
+  grid_launch_dependents();
+  grid_dependency_wait();
   int q_len = p.q_len, kv_len = p.kv_len;
   if (p.q_lens != nullptr) {
     kv_len = min(max(p.kv_lens[b], 0), p.kv_len);
@@ -616,22 +621,24 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     configured = true;
   }
   const dim3 grid(a.B * a.Hq * p.kv_splits, p.n_pairs);
-  if (p.kv_splits == 1) {
-    prefill_kernel<false><<<grid, NTHR, SMEM_BYTES, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHR);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.kv_splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.kv_splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  if (p.kv_splits == 1) {
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<false>, tq, tk, tv, p);
+  }
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tq, tk, tv, p);
 }
 
