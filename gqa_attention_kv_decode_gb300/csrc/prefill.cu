@@ -193,8 +193,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   // Launched with programmatic stream serialisation: the next grid in the
   // stream may start launching at once (its CTAs wait in the same way), and
   // nothing the previous grid writes is read or written before it is done.
+  // With uniform lengths the wait comes after the tensor-memory allocation
+  // and barrier set-up below, which overlap the previous grid's tail; the
+  // per-request lengths are global data, so that case waits here.
   grid_launch_dependents();
-  grid_dependency_wait();
+  if (p.q_lens != nullptr) grid_dependency_wait();
   int q_len = p.q_len, kv_len = p.kv_len;
   if (p.q_lens != nullptr) {
     kv_len = min(max(p.kv_lens[b], 0), p.kv_len);
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  if (p.q_lens == nullptr) grid_dependency_wait();
 
   if (warp >= 8) {
     set_max_regs_dec<REG_CTRL>();
