@@ -55,6 +55,10 @@ __global__ void __launch_bounds__(256) quantize_q4_kernel(const QuantParams p) {
   constexpr int UNR = QuantCfg<D>::UNR;
   constexpr int NG = D / 64;          // groups per row
   const int lane = threadIdx.x & 31;
+  // launched with programmatic stream serialisation: the next grid may start
+  // launching now; the previous one must be complete before any global access
+  grid_launch_dependents();
+  grid_dependency_wait();
   const long long head = blockIdx.y + (long long)gridDim.y * blockIdx.z;
   if (head >= p.heads) return;
   const int row0 = (int(blockIdx.x) * 8 + (int(threadIdx.x) >> 5)) * (RPL * UNR);
@@ -154,10 +158,16 @@ extern "C" GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_he
   // (row blocks of a head, heads): heads spill from y into z past 65535
   const dim3 grid(unsigned((rows + rows_per_cta - 1) / rows_per_cta), unsigned(heads < 65535 ? heads : 65535),
                   unsigned((heads + 65534) / 65535));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 128)
-    quantize_q4_kernel<128><<<grid, 256, 0, s>>>(p);
-  else
-    quantize_q4_kernel<64><<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = D == 128 ? cudaLaunchKernelEx(&cfg, quantize_q4_kernel<128>, p)
+                                 : cudaLaunchKernelEx(&cfg, quantize_q4_kernel<64>, p);
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
