@@ -30,7 +30,13 @@
  *     anything, including NaN.  Every pointer must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous on that stream; the library never
- *     synchronises the device.
+ *     synchronises the device.  Kernels are launched with programmatic
+ *     stream serialisation: each waits (griddepcontrol.wait) for the work
+ *     before it in the stream before touching memory, and lets the next
+ *     kernel begin launching early.  Work that follows in the stream sees the
+ *     results as usual; a caller's own kernel launched with programmatic
+ *     serialisation after a call must itself wait for its predecessor (as
+ *     that launch mode always requires) before reading the outputs.
  *   - The library allocates no device memory.  Scratch memory (the split-KV
  *     partials) is a caller-owned `workspace` whose size the matching
  *     *_workspace_size() call returns for the current device.  Only its first
