@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
       prefetch_l2_bulk(vbase + size_t(row0) * C::ROWB, bytes);
     }
   }
+  if (tid == 32)  // and this CTA's query rows (a prefetch only warms L2; it reads nothing early)
+    prefetch_l2_bulk(static_cast<const T*>(p.q) + (size_t(b) * p.Hq + h0) * D, uint32_t(nh * D * C::E));
   grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;

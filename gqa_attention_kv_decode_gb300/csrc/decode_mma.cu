@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
       prefetch_l2_bulk(p.v + (head_row0 + row0) * D * 2, bytes);
     }
   }
+  if (tid == 32)  // and this CTA's query rows
+    prefetch_l2_bulk(p.q + (size_t(b) * p.Hq + h0) * D, uint32_t(nh * D * 2));
   grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;

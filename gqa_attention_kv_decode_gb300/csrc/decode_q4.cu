@@ -187,6 +187,8 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
       prefetch_l2_bulk(vc + size_t(row0) * C::CB, cbytes);
     }
   }
+  if (tid == 32)  // and this CTA's query rows
+    prefetch_l2_bulk(p.q + (size_t(b) * p.Hq + h0) * D, uint32_t(nh * D * 2));
   grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[b] : p.max_kv_len;
