@@ -867,6 +867,20 @@ def main():
     elapsed_ms = dist.max(t_start.elapsed_time(t_end))
     ms_per_step = elapsed_ms / args.steps
 
+    # the spread of the step times, from K more steps with an event at every
+    # step boundary (outside the region above, which has none)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with torch.cuda.stream(stream):
+        marks[0].record(stream)
+        for i in range(args.steps):
+            time_decode_step(binding, layers, outs, ws, S, stream)
+            marks[i + 1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = sorted(a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:]))
+    step_spread = {"p10": round(step_ms[int(0.1 * (len(step_ms) - 1))], 4),
+                   "p50": round(step_ms[int(0.5 * (len(step_ms) - 1))], 4),
+                   "p90": round(step_ms[int(0.9 * (len(step_ms) - 1))], 4)}
+
     # the same K steps again with every layer call bracketed by events on the
     # launching stream (kept out of the region above: an event pair between
     # calls adds a few microseconds to each)
@@ -949,6 +963,7 @@ def main():
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": LAYERS * args.steps * launches_per_call,
+        "step_ms_spread": step_spread,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
