@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <mutex>
@@ -60,6 +61,7 @@ constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int NST = 4;                          // K/V stages
+constexpr int kMinShareTiles = 6;               // KV tiles per cluster share, at least
 constexpr int OFF_Q = 0;                        // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // NST stages
 constexpr int OFF_V = OFF_K + NST * TILE_BYTES; // NST stages
@@ -72,7 +74,9 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 // one 512-byte run per remote store; the 8 units of a CTA are spread over the
 // cluster.
 constexpr int XCHUNKS = 17, XUNIT = XCHUNKS * 32 * 4;  // floats per unit
-static_assert(8 * XUNIT * 4 <= 2 * NST * TILE_BYTES, "exchange buffer fits in the K/V stages");
+// With ks CTAs in a cluster a rank finishes ceil(8/ks) units; the buffer
+// holds ks of those per rank, at most 14 units (ks = 7).
+static_assert(14 * XUNIT * 4 <= 2 * NST * TILE_BYTES, "exchange buffer fits in the K/V stages");
 // float offset of chunk c of row `lane` in unit (src, slot) of the exchange
 __device__ __forceinline__ int xidx(int src, int slot, int units_per_rank, int c, int lane) {
   return (((src * units_per_rank + slot) * XCHUNKS + c) * 32 + lane) * 4;
@@ -90,7 +94,7 @@ static_assert(OFF_ABORT + 4 <= 256, "barrier area");
 struct PrefillParams {
   __nv_bfloat16* o;
   int Hq, Hkv, n_rep, q_len, kv_len, n_pairs, causal;
-  int kv_splits;        // CTAs of a cluster sharing one pair's KV tiles (1, 2, 4 or 8)
+  int kv_splits;        // CTAs of a cluster sharing one pair's KV tiles (1 to 8)
   float qk_scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int q_pitch;          // rows per head of Q and O
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   // pair rank on y, the longest causal pairs of every head are scheduled
   // first and the short ones fill in behind them.
   const int ks = SPLIT ? p.kv_splits : 1;
+  const int upr = (8 + ks - 1) / ks;  // exchange units a rank finishes
   const int rank = SPLIT ? int(cluster_rank()) : 0;
   const int pair = p.n_pairs - 1 - int(blockIdx.y);
   const int bh = int(blockIdx.x) / ks;  // a cluster = ks consecutive x
@@ -499,7 +504,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       cluster_sync_all();  // every CTA of the cluster is done with its stages
       {
         const int dst_rank = warp % ks, slot = warp / ks;
-        const float* loc = xbuf + xidx(rank, slot, 8 / ks, 0, lane);
+        const float* loc = xbuf + xidx(rank, slot, upr, 0, lane);
         const uint32_t ra = dsmem_addr(loc, uint32_t(dst_rank));
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -524,13 +529,13 @@ __global__ void __launch_bounds__(NTHR, 1)
         __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
         const int slot = warp / ks;
         float M = -INFINITY;
-        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[xidx(src, slot, 8 / ks, 16, lane)]);
+        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[xidx(src, slot, upr, 16, lane)]);
         float w_src[8], L = 0.f;
 #pragma unroll
         for (int src = 0; src < 8; ++src) {
-          const float ms = src < ks ? xbuf[xidx(src, slot, 8 / ks, 16, lane)] : -INFINITY;
+          const float ms = src < ks ? xbuf[xidx(src, slot, upr, 16, lane)] : -INFINITY;
           w_src[src] = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
-          if (src < ks) L += xbuf[xidx(src, slot, 8 / ks, 16, lane) + 1] * w_src[src];
+          if (src < ks) L += xbuf[xidx(src, slot, upr, 16, lane) + 1] * w_src[src];
         }
         const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / L;
 #pragma unroll
@@ -539,8 +544,8 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
           for (int src = 0; src < 8; ++src) {
             if (src < ks) {
-              const float4 v0 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, 8 / ks, 2 * e8, lane));
-              const float4 v1 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, 8 / ks, 2 * e8 + 1, lane));
+              const float4 v0 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, upr, 2 * e8, lane));
+              const float4 v1 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, upr, 2 * e8 + 1, lane));
               const float w = w_src[src];
               acc8[0] += v0.x * w; acc8[1] += v0.y * w; acc8[2] += v0.z * w; acc8[3] += v0.w * w;
               acc8[4] += v1.x * w; acc8[5] += v1.y * w; acc8[6] += v1.z * w; acc8[7] += v1.w * w;
@@ -598,23 +603,24 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.qk_scale_log2 = float(double(a.scale) * 1.4426950408889634);
   p.wait_limit_ns = kWaitLimitNs;
   // Split the KV range of a pair over a cluster when the pairs alone leave
-  // SMs idle: double the CTAs per pair (up to 8) while the grid stays within
-  // one wave and every share keeps at least 8 KV tiles.  (Beyond one wave a
-  // cluster has to wait for SMs of one GPC to free up together, which costs
-  // more than the split gains: T=4097 took 49 us unsplit, 68 us split in two.)
+  // SMs idle: as many CTAs per pair (up to 8) as keep the grid within one
+  // wave and every share at kMinShareTiles KV tiles or more.  (Beyond one
+  // wave a cluster has to wait for SMs of one GPC to free up together, which
+  // costs more than the split gains: T=4097 took 49 us unsplit, 68 us split
+  // in two.)
   {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long pairs = long(a.B) * a.Hq * p.n_pairs;
     const int kv_tiles = (a.kv_len + BN - 1) / BN;
-    int ks = 1;
-    while (ks < 8 && pairs * ks * 2 <= sms && kv_tiles >= 8 * ks) ks *= 2;
-    if (const char* env = std::getenv("GQA_ATTN_PREFILL_KSPLIT")) {  // tuning override: 1, 2, 4 or 8
+    long ks = 1;
+    if (pairs * 2 <= sms) ks = std::min<long>({8L, sms / pairs, std::max<long>(1L, kv_tiles / kMinShareTiles)});
+    if (const char* env = std::getenv("GQA_ATTN_PREFILL_KSPLIT")) {  // tuning override: 1 to 8
       const int v = std::atoi(env);
-      if (v == 1 || v == 2 || v == 4 || v == 8) ks = v;
+      if (v >= 1 && v <= 8) ks = v;
     }
-    p.kv_splits = ks;
+    p.kv_splits = int(ks);
   }
   static bool configured = false;
   if (!configured) {

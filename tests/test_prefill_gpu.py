@@ -117,7 +117,7 @@ def test_growing_scores_force_rescales(causal):
     check_full(q, k, v, T, causal)
 
 
-@pytest.mark.parametrize("ks", [1, 2, 4, 8])
+@pytest.mark.parametrize("ks", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("q_len,kv_len,causal", [(1100, 1100, True), (200, 3000, True), (300, 2000, False),
                                                   (129, 300, True)])
 def test_kv_split_over_cluster(monkeypatch, ks, q_len, kv_len, causal):

@@ -62,7 +62,7 @@ def test_varlen_mix_matches_oracle(causal):
     run_varlen(*MIX, causal=causal, seed=1)
 
 
-@pytest.mark.parametrize("ks", ["1", "2", "4"])
+@pytest.mark.parametrize("ks", ["1", "2", "3", "4", "5"])
 def test_varlen_under_forced_kv_splits(monkeypatch, ks):
     monkeypatch.setenv("GQA_ATTN_PREFILL_KSPLIT", ks)
     run_varlen([200, 33, 512], [3000, 700, 512], seed=2)
