@@ -179,3 +179,20 @@ def test_config_qwen3_4b_ragged_36_layers(B):
             ref = oracle.attention(f64(q[b:b + 1]), f64(k[b:b + 1, :, :L]), f64(v[b:b + 1, :, :L]),
                                    scale=128 ** -0.5)["o"]
             assert np.abs(f64(o[b:b + 1]) - ref).max() <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_back_to_back_calls_read_the_previous_output(dtype):
+    """Each call waits for the grid before it (programmatic dependent launch;
+    only an L2 prefetch of q runs earlier): a second call whose query is the
+    first call's output, on the same stream with no synchronisation and a
+    shared workspace, must see that output complete."""
+    q, k, v = inputs.qkv(1, 28, 4, 128, 1, 4096, dtype, layer=21, device=DEV)
+    _, k2, v2 = inputs.qkv(1, 28, 4, 128, 1, 4096, dtype, layer=22, device=DEV)
+    ws = binding.decode_workspace(1, 28, 4, 128, 4096, binding._dtype_code(q), q.device)
+    o1 = binding.decode(q, k, v, workspace=ws)
+    o2 = binding.decode(o1, k2, v2, workspace=ws)
+    torch.cuda.synchronize()
+    ref2 = oracle.attention(f64(o1), f64(k2), f64(v2), scale=128 ** -0.5)["o"]
+    err = np.abs(f64(o2) - ref2).max()
+    assert err <= TOL[dtype], f"max abs err {err}"

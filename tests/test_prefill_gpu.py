@@ -128,3 +128,21 @@ def test_kv_split_over_cluster(monkeypatch, ks, q_len, kv_len, causal):
     monkeypatch.setenv("GQA_ATTN_PREFILL_KSPLIT", str(ks))
     q, k, v = case(1, 14, 2, q_len, kv_len, layer=ks)
     check_full(q, k, v, kv_len, causal)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(300, 300), (512, 4096)])
+def test_back_to_back_calls_read_the_previous_output(q_len, kv_len):
+    """Launches wait for the grid before them (programmatic dependent launch):
+    a second call whose queries are the first call's output, issued on the
+    same stream with no synchronisation in between, must see that output
+    complete.  (512 queries at 4096 keys takes the cluster-split path.)"""
+    q, k, v = case(1, 14, 2, q_len, kv_len, layer=11)
+    _, k2, v2 = case(1, 14, 2, q_len, kv_len, layer=12)
+    o1 = binding.prefill(q, k, v)
+    o2 = binding.prefill(o1, k2, v2)
+    torch.cuda.synchronize()
+    ref1 = oracle.attention(f64(q), f64(k), f64(v), scale=0.125, causal=True)["o"]
+    assert np.abs(f64(o1) - ref1).max() <= TOL
+    ref2 = oracle.attention(f64(o1), f64(k2), f64(v2), scale=0.125, causal=True)["o"]
+    err = np.abs(f64(o2) - ref2).max()
+    assert err <= TOL, f"max abs err {err}"
