@@ -260,7 +260,8 @@ GQA_ATTN_API int gqa_attn_decode_q4_residual(
  * 15), bias = fp16(min), r = fp32(1 / scale), code = clamp(round_half_even(
  * (x - bias) * r), 0, 15), code 0 when scale == 0, in IEEE fp32 with
  * round-to-nearest operations: the codes are a deterministic function of the
- * input.  The pages give the format
+ * input.  The source is expected to be finite: a NaN element is left out of
+ * its group's minimum and maximum and gets code 0.  The pages give the format
  * x = code * scale + bias but no quantizer; this is the library's reading.
  * Rows of the cache outside [dst_row0, dst_row0 + rows) are not touched.
  * D in {64, 128}; src 16-byte and codes 4-byte aligned, scale and bias
