@@ -745,6 +745,30 @@ def _case_inputs(name, device):
         nbytes = metrics.q4_decode_bytes(32, 8, 128, [S] * 4)
         return (lambda st: binding_mod().gqa_attn_decode_q4(q, *cache, o, None, 128 ** -0.5, ws, max_kv_len=S,
                                                             stream=st)), nbytes, "bytes"
+    if name == "varlen-prefill-B16":
+        B, chunk = 16, 512
+        kv_lens = inputs.ragged_kv_lens(B, chunk, 8192, seed=inputs.BASE_SEED + 7 * B)
+        S = int(kv_lens.max())
+        q = inputs.randn((B, 14, chunk, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+        k = inputs.randn((B, 2, S, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+        v = inputs.randn((B, 2, S, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+        o = torch.empty_like(q)
+        ql = torch.full((B,), chunk, dtype=torch.int32, device=device)
+        kl = torch.from_numpy(kv_lens).to(device)
+        flops = sum(metrics.prefill_flops(14, 64, chunk, int(L), causal=True) for L in kv_lens)
+        return (lambda st: binding_mod().gqa_attn_prefill_varlen(q, k, v, o, ql, kl, 0.125, True, st)), flops, "flop"
+    if name == "decode-f32-layers8-S32768":
+        NL = 8
+        q = inputs.randn((NL, 1, HQ, 1, D), inputs.tensor_seed(0, 0), torch.float32, device)
+        k = inputs.randn((NL, 1, HKV, S_HEAD, D), inputs.tensor_seed(0, 1), torch.float32, device)
+        v = inputs.randn((NL, 1, HKV, S_HEAD, D), inputs.tensor_seed(0, 2), torch.float32, device)
+        o = torch.empty_like(q)
+        ws = torch.zeros(binding_mod().gqa_attn_decode_layers_workspace_size(NL, 1, HQ, HKV, D, S_HEAD,
+                                                                              binding_mod().GQA_F32),
+                         dtype=torch.uint8, device=device)
+        nbytes = NL * metrics.decode_bytes(HQ, HKV, D, [S_HEAD], 4)
+        return (lambda st: binding_mod().gqa_attn_decode_layers(q, k, v, o, None, D ** -0.5, ws, max_kv_len=S_HEAD,
+                                                                stream=st)), nbytes, "bytes"
     if name.startswith("prefill-"):
         parts = name.split("-")[1:]           # prefill-T4097 or prefill-q512-kv4096
         if len(parts) == 1:
@@ -762,7 +786,8 @@ def _case_inputs(name, device):
 
 KERNEL_CASES = ("decode-f32-S32768", "decode-bf16-S32768", "decode-bf16-ragged-B64", "decode-bf16-paged-B64",
                 "q4-B4-S16384", "quantize-B4-S16384",
-                "prefill-T4097", "prefill-T16384", "prefill-q512-kv4096")
+                "prefill-T4097", "prefill-T16384", "prefill-q512-kv4096", "varlen-prefill-B16",
+                "decode-f32-layers8-S32768")
 
 
 def binding_mod():
