@@ -8,11 +8,22 @@
 //
 // Per group of 64 consecutive elements along D (the pages give the format
 // x = code * scale + bias and no quantizer; the reading used everywhere in
-// this library): scale = fp16((max - min) / 15), bias = fp16(min), r = the
-// fp32 reciprocal of the scale, code = clamp(round_half_even((x - bias) * r),
-// 0, 15), 0 when the scale is 0.  The arithmetic is IEEE fp32 with
-// round-to-nearest operations, so the integer codes are a deterministic
-// function of the input.
+// this library): scale = fp16((max - min) / 15), bias = fp16(min),
+// code = clamp(round_half_even((x - bias) / scale), 0, 15), 0 when the scale
+// is 0, with the subtraction and the division each one IEEE fp32 operation
+// rounded to nearest.  The codes are a deterministic function of the input.
+//
+// The division is formed without a divide instruction.  With y = RN(1/s),
+// q0 = RN(d y) is within 2^-22 |q| of the exact quotient q = d / s, and one
+// residual step q1 = RN(q0 + RN(d - s q0) y) (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990) brings the value before its last rounding within about
+// 2^-44 |q| of q.  That last rounding returns RN(q), because q is never that
+// close to a midpoint mid between two consecutive floats: d has 24 significant
+// bits and s (fp16) 11, so d - mid s is a nonzero multiple of
+// 2^(e_q + e_s - 34) and |q - mid| >= 2^(e_q - 35).  So q1 is exactly the
+// quotient a correctly rounded fp32 division returns, and the ties of
+// round-half-even are decided on the same value.
 //
 // A lane loads 16 bytes (8 elements); D/8 lanes hold a row and 8 lanes a
 // group, whose minimum and maximum come from three xor shuffles.  A warp keeps
@@ -95,14 +106,20 @@ __global__ void __launch_bounds__(256) quantize_q4_kernel(const QuantParams p) {
     const __half b16 = __float2half_rn(lo);
     const float s = __half2float(s16), bb = __half2float(b16);
     const float rcp = __frcp_rn(s);
-    // per pair: (x - bias) * r (x + (-bias) is x - bias), rounded to the
-    // nearest integer, ties to even, by the saturating conversion (negative
-    // values and NaN give 0), then capped at 15
-    const float2 nb = make_float2(-bb, -bb), r2 = make_float2(rcp, rcp);
+    // with an infinite scale or bias the quotients are 0, +-inf or NaN, which
+    // the reciprocal product already gives exactly; the residual step would
+    // turn them into NaN
+    const bool corr = fabsf(s) < INFINITY && fabsf(bb) < INFINITY;
+    // per pair: d = x - bias (x + (-bias) is x - bias), q = d / scale as
+    // above, rounded to the nearest integer, ties to even, by the saturating
+    // conversion (negative values and NaN give 0), then capped at 15
+    const float2 nb = make_float2(-bb, -bb), r2 = make_float2(rcp, rcp), ns2 = make_float2(-s, -s);
     uint32_t packed = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 t = __fmul2_rn(__fadd2_rn(bf16x2_to_float2(ww[i]), nb), r2);
+      const float2 d = __fadd2_rn(bf16x2_to_float2(ww[i]), nb);
+      float2 t = __fmul2_rn(d, r2);
+      if (corr) t = __ffma2_rn(__ffma2_rn(t, ns2, d), r2, t);
       const uint32_t k0 = min(__float2uint_rn(t.x), 15u), k1 = min(__float2uint_rn(t.y), 15u);
       packed += (k0 + 16u * k1) << (8 * i);
     }

@@ -35,10 +35,11 @@ design notes):
     dequantises them and calls SDPA -- this module is that baseline);
   * the 4-bit quantizer (the pages say "group-affine", x = code*scale + bias,
     and give no quantizer): per group, scale = fp16((max - min) / 15),
-    bias = fp16(min), r = fp32(1 / scale), code = clamp(round_half_even((x -
-    bias) * r), 0, 15), code 0 when scale == 0; computed in float32, the
-    precision in which the GPU kernel takes the same integer decisions (one
-    reciprocal per group rather than a division per element);
+    bias = fp16(min), code = clamp(round_half_even((x - bias) / scale), 0,
+    15), code 0 when scale == 0.  The code inverts the dequantisation
+    formula directly: one IEEE float32 subtraction and one correctly rounded
+    float32 division per element (float32 is the precision the bf16 source
+    and the fp16 scale and bias widen to exactly), then round half to even;
   * the residual window of a 4-bit cache (the pages: a production KIVI cache
     keeps the most recent tokens unquantized): key rows [0, n_quant[b]) of
     request b come from the 4-bit cache and rows [n_quant[b], kv_lens[b])
@@ -52,6 +53,8 @@ design notes):
 """
 
 from __future__ import annotations
+
+import warnings
 
 import numpy as np
 
@@ -236,29 +239,33 @@ def quantize_q4(x, group_size: int = 64):
     """Group-affine 4-bit quantization of x [..., D] (float32 arithmetic).
 
     Per group of ``group_size`` consecutive elements along D: the minimum and
-    maximum m, M; scale = fp16((M - m) / 15) and bias = fp16(m) (round to
-    nearest); r = 1 / scale rounded to float32; code = round-half-even((x -
-    bias) * r) clamped to [0, 15], and 0 where the scale is 0.  Codes are packed two per byte, element 2t in
-    the low nibble of byte t.  Returns (codes uint8 [..., D/2], scale fp16,
-    bias fp16 [..., D/group_size]).  ("Batching Decode Attention Across
-    Requests ...", VeloxQuant-MLX blog, "Part 4": the cache is quantized
-    incrementally, one newly aged group-aligned block per step.)
+    maximum m, M (NaN elements left out); scale = fp16((M - m) / 15) and
+    bias = fp16(m) (round to nearest); code = round-half-even((x - bias) /
+    scale) with the subtraction and the division each one IEEE float32
+    operation, clamped to [0, 15]; code 0 where the scale is 0 or the
+    quotient is NaN.  Codes are packed two per byte, element 2t in the low
+    nibble of byte t.  Returns (codes uint8 [..., D/2], scale fp16, bias fp16
+    [..., D/group_size]).  ("Batching Decode Attention Across Requests ...",
+    VeloxQuant-MLX blog, "Part 4": the format x = code * scale + bias, and a
+    cache quantized incrementally, one newly aged group-aligned block per
+    step.)
     """
     x = np.asarray(x, dtype=np.float32)
     D = x.shape[-1]
     if D % group_size != 0 or D % 2 != 0:
         raise ValueError("D must be a multiple of the group size")
     grp = x.reshape(x.shape[:-1] + (D // group_size, group_size))
-    lo = grp.min(axis=-1)
-    hi = grp.max(axis=-1)
-    scale = ((hi - lo) / np.float32(15.0)).astype(np.float16)
-    bias = lo.astype(np.float16)
-    s32 = scale.astype(np.float32)[..., None]
-    b32 = bias.astype(np.float32)[..., None]
-    with np.errstate(divide="ignore", invalid="ignore"):
-        r32 = np.float32(1.0) / s32
-        q = np.rint((grp - b32) * r32)
-    q = np.where(s32 > 0, np.clip(q, 0, 15), 0).astype(np.uint8).reshape(x.shape)
+    with np.errstate(all="ignore"), warnings.catch_warnings():
+        warnings.simplefilter("ignore", RuntimeWarning)  # an all-NaN group has a NaN scale
+        lo = np.nanmin(grp, axis=-1)
+        hi = np.nanmax(grp, axis=-1)
+        scale = ((hi - lo) / np.float32(15.0)).astype(np.float16)
+        bias = lo.astype(np.float16)
+        s32 = scale.astype(np.float32)[..., None]
+        b32 = bias.astype(np.float32)[..., None]
+        q = np.rint((grp - b32) / s32)
+        q = np.where(np.isnan(q), np.float32(0), np.clip(q, 0, 15))
+    q = np.where(s32 > 0, q, 0).astype(np.uint8).reshape(x.shape)
     packed = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
     return packed, scale, bias
 

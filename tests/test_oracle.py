@@ -444,6 +444,21 @@ def test_pins_catch_quantizer_slips(monkeypatch):
     assert not np.array_equal(swapped, np.array(case["codes"], dtype=np.uint8))
 
 
+def test_pin_separates_division_from_reciprocal():
+    """A quantizer that multiplies by the fp32 reciprocal of the scale instead
+    of dividing by it fails the 'division_ties_not_reciprocal' hand case."""
+    case = next(c for c in _cases()["quantizer_cases"] if c["name"] == "division_ties_not_reciprocal")
+    x = np.array(case["x"], dtype=np.float32)
+    c, _, _ = oracle.quantize_q4(x)
+    np.testing.assert_array_equal(c, np.array(case["codes"], dtype=np.uint8))
+    # the same group, quotients formed with the reciprocal
+    s = np.float32(case["scale"][0])
+    alt = np.clip(np.rint(x * (np.float32(1.0) / s)), 0, 15).astype(np.uint8)
+    alt_packed = alt[0::2] | (alt[1::2] << 4)
+    assert not np.array_equal(alt_packed, np.array(case["codes"], dtype=np.uint8))
+    assert alt_packed[:3].tolist() == [240, 215, 63]
+
+
 # --- 4-bit cache with an unquantized residual window ------------------------------
 
 @pytest.mark.parametrize("case", _cases()["residual_cases"], ids=lambda c: c["name"])

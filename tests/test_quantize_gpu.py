@@ -120,3 +120,48 @@ def test_quantizer_more_heads_than_one_grid_row():
     binding.gqa_attn_quantize_q4(x, codes, scale, bias, dst_row0=0)
     torch.cuda.synchronize()
     check_rows(x, codes, scale, bias, 0)
+
+
+def _tie_groups(n_groups, seed):
+    """Groups whose quotients (x - bias) / scale sit on or next to half-integers.
+
+    Per group: scale s with 3 significant bits (exact in fp16 and bf16), bias
+    lo = -j s, maximum lo + 15 s, so that the group's own scale and bias are
+    s and lo; then 40 values lo + (k + 1/2) s (exact ties), 10 bf16 neighbours
+    of such ties and 12 values drawn inside [lo, lo + 15 s].
+    """
+    rng = np.random.default_rng(seed)
+    out = np.empty((n_groups, 64), dtype=np.float32)
+    for g in range(n_groups):
+        s = np.float32((8 + rng.integers(0, 8)) * 2.0 ** int(rng.integers(-12, 7)) / 8)
+        lo = np.float32(-int(rng.integers(0, 4)) * s)
+        k = rng.integers(0, 15, 50).astype(np.float32)
+        ties = lo + (k + np.float32(0.5)) * s
+        vals = np.concatenate([[lo, lo + 15 * s], ties,
+                               lo + rng.uniform(0, 15, 12).astype(np.float32) * s])
+        vals = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16)
+        bits = vals.view(torch.int16)
+        bits[42:52] += torch.from_numpy(rng.choice([-1, 1], 10).astype(np.int16))  # bf16 neighbours
+        vals = bits.view(torch.bfloat16).float().numpy()
+        out[g] = np.clip(vals, lo, lo + 15 * s)[rng.permutation(64)]
+    return out
+
+
+def test_quantizer_ties_bit_for_bit():
+    """Codes on and next to the round-half-even ties: the GPU's quotient must
+    be the correctly rounded fp32 division, not the reciprocal product."""
+    x = _tie_groups(2048, 123)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    assert torch.equal(xb.float(), torch.from_numpy(x))  # every value is exact in bf16
+    src = xb.view(1, 2048, 1, 64).to(DEV)
+    codes, scale, bias = empty_cache(1, 2048, 1, 64)
+    binding.gqa_attn_quantize_q4(src, codes, scale, bias)
+    torch.cuda.synchronize()
+    check_rows(src, codes, scale, bias, 0)
+    # the same groups quantized with the reciprocal product differ somewhere,
+    # so this test separates the two readings
+    c, s_ref, b_ref = oracle.quantize_q4(x)
+    s32, b32 = s_ref.astype(np.float32), b_ref.astype(np.float32)
+    alt = np.clip(np.rint((x - b32) * (np.float32(1.0) / s32)), 0, 15).astype(np.uint8)
+    alt = alt[:, 0::2] | (alt[:, 1::2] << 4)
+    assert (alt != c).any()
