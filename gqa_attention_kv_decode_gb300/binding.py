@@ -10,6 +10,7 @@ not been built, the first call raises instead of falling back to anything.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -53,6 +54,9 @@ EXPORTED = (
     "gqa_attn_clear_device_status",
     "gqa_attn_decode_num_splits",
     "gqa_attn_version",
+    "gqa_attn_set_plan_override",
+    "gqa_attn_read_prefill_status",
+    "gqa_attn_clear_prefill_status",
 )
 
 _lib = None
@@ -117,6 +121,12 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode_num_splits.restype = i32
     L.gqa_attn_version.argtypes = []
     L.gqa_attn_version.restype = i32
+    L.gqa_attn_set_plan_override.argtypes = [i32, i32]
+    L.gqa_attn_set_plan_override.restype = i32
+    L.gqa_attn_read_prefill_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    L.gqa_attn_read_prefill_status.restype = i32
+    L.gqa_attn_clear_prefill_status.argtypes = [vp]
+    L.gqa_attn_clear_prefill_status.restype = i32
     _lib = L
     return L
 
@@ -158,6 +168,23 @@ def gqa_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
 
 def gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
     return lib().gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype)
+
+
+def gqa_attn_set_plan_override(decode_splits=0, prefill_kv_split=0) -> None:
+    """Tuning and tests only: force the decode split count and the prefill
+    KV-split cluster size (0 = the planner's choice)."""
+    _check(lib().gqa_attn_set_plan_override(int(decode_splits), int(prefill_kv_split)),
+           "gqa_attn_set_plan_override")
+
+
+@contextlib.contextmanager
+def plan_override(decode_splits=0, prefill_kv_split=0):
+    """``with plan_override(...)``: the override for the block, then none."""
+    gqa_attn_set_plan_override(decode_splits, prefill_kv_split)
+    try:
+        yield
+    finally:
+        gqa_attn_set_plan_override(0, 0)
 
 
 def gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len=None, stream=None):
@@ -324,6 +351,17 @@ def gqa_attn_read_device_status(workspace, stream=None) -> int:
 def gqa_attn_clear_device_status(workspace, stream=None):
     _check(lib().gqa_attn_clear_device_status(_ptr(workspace), _stream(stream)),
            "gqa_attn_clear_device_status")
+
+
+def gqa_attn_read_prefill_status(stream=None) -> int:
+    out = ctypes.c_uint32(0)
+    _check(lib().gqa_attn_read_prefill_status(ctypes.byref(out), _stream(stream)),
+           "gqa_attn_read_prefill_status")
+    return out.value
+
+
+def gqa_attn_clear_prefill_status(stream=None):
+    _check(lib().gqa_attn_clear_prefill_status(_stream(stream)), "gqa_attn_clear_prefill_status")
 
 
 def gqa_attn_version() -> int:

@@ -3,8 +3,8 @@
 // runs on the host before anything is launched.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
-#include <cstdlib>
 #include <mutex>
 
 #include "gqa_attn.h"
@@ -26,11 +26,18 @@ int device_sm_count() {
 
 static long ceil_div(long a, long b) { return (a + b - 1) / b; }
 
+// Plan overrides (gqa_attn_set_plan_override); 0 = the planner decides.
+static std::atomic<int> g_decode_splits_override{0};
+static std::atomic<int> g_prefill_kv_split_override{0};
+
+int prefill_kv_split_override() { return g_prefill_kv_split_override.load(std::memory_order_relaxed); }
+
 // Chooses how many key splits each (request, KV head) gets so that the grid
 // covers at most ctas_per_sm CTAs per SM (one wave) when requests are few and
 // short, while a split stays at least one tile and at most 1024 rows long (so
-// the splits of long, ragged requests balance across the SMs).  GQA_ATTN_SPLITS, when
-// set, forces the split count (tuning only).
+// the splits of long, ragged requests balance across the SMs).  A split count
+// set with gqa_attn_set_plan_override (tuning and tests only) replaces the
+// planner's choice.
 SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_sms, int ctas_per_sm) {
   SplitPlan p;
   const int n_rep = Hq / Hkv;
@@ -51,10 +58,8 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   // two tiles or fewer: one CTA per head group is faster than a split plus
   // its merge kernel
   if (max_kv_len <= 2L * tile) chunk = ceil_div(max_kv_len, tile) * tile;
-  if (const char* env = std::getenv("GQA_ATTN_SPLITS")) {
-    const long n = std::atol(env);
-    if (n > 0) chunk = ceil_div(max_kv_len, n);
-  }
+  if (const int n = g_decode_splits_override.load(std::memory_order_relaxed); n > 0)
+    chunk = ceil_div(max_kv_len, n);
   if (chunk < lo) chunk = lo;
   if (ceil_div(max_kv_len, chunk) > 1024) chunk = ceil_div(max_kv_len, 1024);
   p.chunk = int(chunk);
@@ -111,9 +116,35 @@ size_t decode_ws_size(int B, int Hq, int Hkv, int D, int max_kv_len, int tile, i
 
 }  // namespace
 
+// Shape, dtype and pointer checks of a contiguous-cache decode call, in the
+// order gqa_attn_decode applies them (the workspace is checked separately).
+int gqa::validate_decode_args(const void* q, const void* k, const void* v, const void* o,
+                              const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int S_cap,
+                              int max_kv_len, float scale, int dtype) {
+  int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_kv_len, scale);
+  if (rc != GQA_OK) return rc;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  rc = check_ptrs({q, k, v, o}, dev, 16);
+  if (rc != GQA_OK) return rc;
+  if (kv_lens != nullptr) {
+    rc = check_ptrs({kv_lens}, dev, 4);
+    if (rc != GQA_OK) return rc;
+  }
+  return GQA_OK;
+}
+
 extern "C" {
 
 GQA_ATTN_API int gqa_attn_version(void) { return 100; }
+
+GQA_ATTN_API int gqa_attn_set_plan_override(int decode_splits, int prefill_kv_split) {
+  if (decode_splits < 0 || prefill_kv_split < 0 || prefill_kv_split > 8) return GQA_ERR_INVALID_ARG;
+  g_decode_splits_override.store(decode_splits, std::memory_order_relaxed);
+  g_prefill_kv_split_override.store(prefill_kv_split, std::memory_order_relaxed);
+  return GQA_OK;
+}
 
 GQA_ATTN_API const char* gqa_attn_status_string(int status) {
   switch (status) {
@@ -147,17 +178,10 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
                                  const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int S_cap,
                                  int max_kv_len, float scale, int dtype, void* workspace,
                                  size_t ws_bytes, void* stream) {
-  int rc = check_decode_shape(B, Hq, Hkv, D, S_cap, max_kv_len, scale);
+  int rc = gqa::validate_decode_args(q, k, v, o, kv_lens, B, Hq, Hkv, D, S_cap, max_kv_len, scale, dtype);
   if (rc != GQA_OK) return rc;
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
-  rc = check_ptrs({q, k, v, o}, dev, 16);
-  if (rc != GQA_OK) return rc;
-  if (kv_lens != nullptr) {
-    rc = check_ptrs({kv_lens}, dev, 4);
-    if (rc != GQA_OK) return rc;
-  }
   if (workspace == nullptr) return GQA_ERR_WORKSPACE;
   rc = check_ptrs({workspace}, dev, 256);
   if (rc == GQA_ERR_INVALID_ARG) return GQA_ERR_WORKSPACE;

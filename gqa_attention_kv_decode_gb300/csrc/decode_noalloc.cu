@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "gqa_attn.h"
+#include "internal.h"
 
 namespace {
 
@@ -39,7 +40,10 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (set up on the
-// first call per device).
+// first call per device and kept for the life of the process).  The cached
+// address belongs to the device's primary context, the one the CUDA runtime
+// uses; after cudaDeviceReset, or with another driver-API context current,
+// it no longer names the array.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
@@ -63,6 +67,11 @@ extern "C" GQA_ATTN_API int gqa_attn_decode_noalloc(const void* q, const void* k
                                                     void* o, const int32_t* kv_lens, int B, int Hq,
                                                     int Hkv, int D, int S_cap, int max_kv_len,
                                                     float scale, int dtype, void* stream) {
+  // the checks of gqa_attn_decode first, so that an invalid call gets the
+  // same error code from both entry points
+  const int valid = gqa::validate_decode_args(q, k, v, o, kv_lens, B, Hq, Hkv, D, S_cap, max_kv_len, scale,
+                                              dtype);
+  if (valid != GQA_OK) return valid;
   const size_t need = gqa_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, dtype);
   if (need == 0) return GQA_ERR_INVALID_ARG;
   if (need > kScratchBytes) return GQA_ERR_SCRATCH_LIMIT;

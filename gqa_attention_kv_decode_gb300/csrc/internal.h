@@ -45,6 +45,15 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
 
 int device_sm_count();
 
+// The prefill KV-split cluster size forced by gqa_attn_set_plan_override, or
+// 0 (the planner decides).
+int prefill_kv_split_override();
+
+// Shape, dtype and pointer checks shared by gqa_attn_decode and
+// gqa_attn_decode_noalloc (everything but the workspace); GQA_OK or an error.
+int validate_decode_args(const void* q, const void* k, const void* v, const void* o, const int32_t* kv_lens,
+                         int B, int Hq, int Hkv, int D, int S_cap, int max_kv_len, float scale, int dtype);
+
 struct DecodeArgs {
   const void* q;
   const void* k;

@@ -86,10 +86,16 @@ __device__ __forceinline__ int xidx(int src, int slot, int units_per_rank, int c
 //   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
 //   B_P0[t]  P_t keys 0..63 stored            B_P1[t]  P_t keys 64..127 stored
 //   B_O0[t]  P.V over keys 0..63 done         B_O1[t]  P.V over all keys done
+//   B_DRAIN  after a timed-out wait: the MMA-issuing warps' work is done
 constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST, B_SC = B_S + 2,
-              B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2, N_BARS = B_O1 + 2;
+              B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2, B_DRAIN = B_O1 + 2,
+              N_BARS = B_DRAIN + 1;
 constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8;
 static_assert(OFF_ABORT + 4 <= 256, "barrier area");
+
+// Status of the prefill calls on this device (GQA_DEV_* bits), OR-accumulated
+// by every prefill kernel until gqa_attn_clear_prefill_status.
+__device__ uint32_t g_prefill_status = 0;
 
 struct PrefillParams {
   __nv_bfloat16* o;
@@ -205,8 +211,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (p.q_lens != nullptr) grid_dependency_wait();
   int q_len = p.q_len, kv_len = p.kv_len;
   if (p.q_lens != nullptr) {
-    kv_len = min(max(p.kv_lens[b], 0), p.kv_len);
-    q_len = min(max(p.q_lens[b], 0), min(p.q_len, kv_len));
+    const int kv_raw = p.kv_lens[b], q_raw = p.q_lens[b];
+    kv_len = min(max(kv_raw, 0), p.kv_len);
+    q_len = min(max(q_raw, 0), min(p.q_len, kv_len));
+    if (threadIdx.x == 0 && blockIdx.y == 0 && (kv_raw != kv_len || q_raw != q_len))
+      atomicOr(&g_prefill_status, GQA_DEV_KVLEN_CLAMPED);
     // a pair past this request's queries has nothing to do (the CTAs of a
     // cluster share the pair, so they leave together)
     if (m0 >= q_len) return;
@@ -241,8 +250,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (tid == 256) {
     for (int i = 0; i < N_BARS; ++i) {
       const bool per_warp = (i >= B_SC && i < B_O0);  // arrivals of the 4 softmax warps of a tile
-      const bool stage_free = (i >= B_KE && i < B_KE + NST);  // the three MMA-issuing warps
-      mbar_init(&bars[i], per_warp ? 4 : stage_free ? 3 : 1);
+      const bool three = (i >= B_KE && i < B_KE + NST) || i == B_DRAIN;  // the three MMA-issuing warps
+      mbar_init(&bars[i], per_warp ? 4 : three ? 3 : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -564,6 +573,19 @@ __global__ void __launch_bounds__(NTHR, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // After a wait that timed out, tensor-core work may still be in flight:
+  // the three issuing warps wait (bounded) for all of their own before the
+  // tensor memory is released, and the call is flagged.  (Otherwise every
+  // MMA has been waited for by the softmax warps already.)
+  if (*abort_flag) {
+    if (warp >= 9 && warp <= 11) {
+      mma_commit_warp(&bars[B_DRAIN]);
+      mbar_wait_bounded(&bars[B_DRAIN], 0, p.wait_limit_ns);
+    }
+    if (tid == 0) atomicOr(&g_prefill_status, GQA_DEV_WAIT_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 9) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -616,10 +638,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     const int kv_tiles = (a.kv_len + BN - 1) / BN;
     long ks = 1;
     if (pairs * 2 <= sms) ks = std::min<long>({8L, sms / pairs, std::max<long>(1L, kv_tiles / kMinShareTiles)});
-    if (const char* env = std::getenv("GQA_ATTN_PREFILL_KSPLIT")) {  // tuning override: 1 to 8
-      const int v = std::atoi(env);
-      if (v >= 1 && v <= 8) ks = v;
-    }
+    if (const int v = prefill_kv_split_override(); v >= 1 && v <= 8) ks = v;  // tuning and tests only
     p.kv_splits = int(ks);
   }
   static bool configured = false;
@@ -653,3 +672,25 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace gqa
+
+using namespace gqa;
+
+extern "C" GQA_ATTN_API int gqa_attn_read_prefill_status(uint32_t* out, void* stream) {
+  if (out == nullptr) return GQA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyFromSymbolAsync(out, g_prefill_status, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+extern "C" GQA_ATTN_API int gqa_attn_clear_prefill_status(void* stream) {
+  static const uint32_t zero = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyToSymbolAsync(g_prefill_status, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}

@@ -257,10 +257,10 @@ GQA_ATTN_API int gqa_attn_decode_q4_residual(
  *   scale,  fp16 [heads, dst_head_rows, D/64]   (written)
  *   bias
  * Per group of group_size = 64 elements along D: scale = fp16((max - min) /
- * 15), bias = fp16(min), r = fp32(1 / scale), code = clamp(round_half_even(
- * (x - bias) * r), 0, 15), code 0 when scale == 0, in IEEE fp32 with
- * round-to-nearest operations: the codes are a deterministic function of the
- * input.  The source is expected to be finite: a NaN element is left out of
+ * 15), bias = fp16(min), code = clamp(round_half_even((x - bias) / scale), 0,
+ * 15), code 0 when scale == 0, where x - bias and the quotient are each the
+ * correctly rounded IEEE fp32 result: the codes are a deterministic function
+ * of the input, the direct inverse of x = code * scale + bias.  The source is expected to be finite: a NaN element is left out of
  * its group's minimum and maximum and gets code 0.  The pages give the format
  * x = code * scale + bias but no quantizer; this is the library's reading.
  * Rows of the cache outside [dst_row0, dst_row0 + rows) are not touched.
@@ -274,6 +274,23 @@ GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_head_rows, ui
                                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Plan overrides, for tuning and tests only.
+ *
+ * decode_splits > 0 makes every later decode call (all decode entry points
+ * and their *_workspace_size queries) cut each request's keys into that many
+ * splits instead of the planner's count (a split still holds at least one
+ * tile, and there are at most 1024).  prefill_kv_split in [1, 8] forces the
+ * size of the thread-block cluster that shares one query-tile pair's keys in
+ * prefill (1 = no split).  0 restores the planner's choice for either.  The
+ * setting is process-wide and starts at 0; nothing else (no environment
+ * variable) changes a plan.  Change it only while no other thread is calling
+ * the library, and size workspaces after changing it.
+ * Returns GQA_OK, or GQA_ERR_INVALID_ARG for a negative value or a
+ * prefill_kv_split above 8.
+ * ------------------------------------------------------------------------- */
+GQA_ATTN_API int gqa_attn_set_plan_override(int decode_splits, int prefill_kv_split);
+
+/* ---------------------------------------------------------------------------
  * Single-token decode without any caller-provided or allocated scratch.
  *
  * There is no counterpart of this entry point in the pages; it exists for
@@ -285,7 +302,12 @@ GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_head_rows, ui
  * loads the library holds that array until the process exits.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process and belongs to the device's primary context (the one the CUDA
+ *     runtime uses): after cudaDeviceReset, or from another driver-API
+ *     context, do not call this entry point again in the same process.
+ *   - Arguments are checked as gqa_attn_decode checks them, with the same
+ *     error codes, before the size limit below.
  *   - Problems whose workspace (gqa_attn_decode_workspace_size) exceeds the
  *     array are rejected with GQA_ERR_SCRATCH_LIMIT before anything runs.
  *   - All calls share the array.  Calls whose GPU work may overlap (other
@@ -348,6 +370,12 @@ GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes,
  *   limits   q_len <= 65535 * 256, B * Hq < 2^31 (else GQA_ERR_INVALID_ARG).
  * Errors: as for decode; a dtype / D without a kernel is GQA_ERR_UNSUPPORTED.
  * Nothing is allocated; the call is asynchronous on `stream`.
+ * Device-side anomalies of both prefill entry points go to the prefill
+ * status word of the device (see gqa_attn_read_prefill_status): a tile copy
+ * that does not arrive within the kernel's bounded wait sets
+ * GQA_DEV_WAIT_TIMEOUT and the affected output rows are written as NaN
+ * (never as plausible values); per-request lengths that had to be clamped
+ * (varlen) set GQA_DEV_KVLEN_CLAMPED.
  * ------------------------------------------------------------------------- */
 GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, void* o,
                                   int B, int Hq, int Hkv, int D, int q_len, int kv_len,
@@ -367,6 +395,17 @@ GQA_ATTN_API int gqa_attn_read_device_status(const void* workspace, uint32_t* ou
 
 /* Zeroes the device status word of `workspace` (asynchronous on `stream`). */
 GQA_ATTN_API int gqa_attn_clear_device_status(void* workspace, void* stream);
+
+/* Prefill has no workspace; its device status lives in the library: one
+ * 32-bit word per device (GQA_DEV_* bits, starting at 0), OR-accumulated by
+ * every gqa_attn_prefill / gqa_attn_prefill_varlen kernel on that device,
+ * whatever its stream, until cleared.  read copies it to *out after the work
+ * queued on `stream` so far has finished (synchronises that stream; out must
+ * not be NULL); clear zeroes it in stream order and also synchronises.  For
+ * flags per call, clear before the call and read after it on the same
+ * stream, with no other prefill running on the device in between. */
+GQA_ATTN_API int gqa_attn_read_prefill_status(uint32_t* out, void* stream);
+GQA_ATTN_API int gqa_attn_clear_prefill_status(void* stream);
 
 /* Number of splits along the keys the decode entry points use for this
  * problem on the current device (the grid's x extent); exposed for tests. */

@@ -93,3 +93,22 @@ def test_prefill_rejects_bad_causal_flag(lib):
 def test_workspace_size_is_zero_for_invalid_shapes(lib):
     assert binding.gqa_attn_decode_workspace_size(1, 14, 3, 64, 128, 0) == 0
     assert binding.gqa_attn_decode_workspace_size(1, 14, 2, 64, 128, 0) > 0
+
+
+def test_plan_override_checks_its_arguments(lib):
+    assert lib.gqa_attn_set_plan_override(-1, 0) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_set_plan_override(0, 9) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_set_plan_override(0, -2) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_set_plan_override(0, 0) == binding.GQA_OK
+
+
+def test_plan_override_is_not_read_from_the_environment(lib, monkeypatch):
+    """Only the explicit call changes a plan: the split count the planner
+    reports does not move when a tuning-looking variable is set."""
+    before = lib.gqa_attn_decode_workspace_size(1, 28, 4, 128, 32768, 0)
+    monkeypatch.setenv("GQA_ATTN_SPLITS", "3")
+    assert lib.gqa_attn_decode_workspace_size(1, 28, 4, 128, 32768, 0) == before
+
+
+def test_read_prefill_status_rejects_a_null_output(lib):
+    assert lib.gqa_attn_read_prefill_status(None, None) == binding.GQA_ERR_INVALID_ARG

@@ -74,10 +74,10 @@ def test_ragged_batch_with_poisoned_tails(dtype):
 
 
 @pytest.mark.parametrize("splits", ["1", "3", "16", "1000"])
-def test_forced_split_counts(monkeypatch, splits):
-    monkeypatch.setenv("GQA_ATTN_SPLITS", splits)
+def test_forced_split_counts(splits):
     q, k, v = inputs.qkv(2, 28, 4, 128, 1, 1000, torch.float32, layer=5, device=DEV)
-    o = run_decode(q, k, v, kv_lens=[1000, 517])
+    with binding.plan_override(decode_splits=int(splits)):
+        o = run_decode(q, k, v, kv_lens=[1000, 517])
     check(q, k, v, o, kv_lens=[1000, 517])
 
 

@@ -83,12 +83,12 @@ def test_paged_decode_matches_oracle(dtype, D, block_size, append, Hq, Hkv):
 
 @pytest.mark.parametrize("splits", ["1", "3", "7", "40"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
-def test_paged_append_under_forced_split_counts(monkeypatch, splits, dtype):
+def test_paged_append_under_forced_split_counts(splits, dtype):
     """The CTA that owns the appended row depends on the split count."""
-    monkeypatch.setenv("GQA_ATTN_SPLITS", splits)
     kv_lens = [3000, 1500, 65, 64, 129]
     q, kp, vp, table, kn, vn = make(len(kv_lens), 28, 4, 128, 3000, kv_lens, dtype, 64, 11, True)
-    run_and_check(q, kp, vp, table, kn, vn, kv_lens, 3000, 64)
+    with binding.plan_override(decode_splits=int(splits)):
+        run_and_check(q, kp, vp, table, kn, vn, kv_lens, 3000, 64)
 
 
 def test_paged_qwen3_4b_ragged_B16_bf16():

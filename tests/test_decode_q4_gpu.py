@@ -73,10 +73,10 @@ def test_q4_ragged_with_poisoned_tails():
 
 
 @pytest.mark.parametrize("splits", ["1", "5", "64"])
-def test_q4_forced_split_counts(monkeypatch, splits):
-    monkeypatch.setenv("GQA_ATTN_SPLITS", splits)
+def test_q4_forced_split_counts(splits):
     q, cache = make_case(2, 32, 8, 128, 4096, layer=9)
-    o = run(q, cache, kv_lens=[4096, 1500])
+    with binding.plan_override(decode_splits=int(splits)):
+        o = run(q, cache, kv_lens=[4096, 1500])
     assert np.abs(o.float().cpu().numpy() - oracle_o(q, cache, [4096, 1500], 128)).max() <= TOL
 
 

@@ -71,11 +71,11 @@ def test_q4_residual_matches_oracle(D, R_cap, Hq, Hkv):
 
 
 @pytest.mark.parametrize("splits", ["1", "4", "33"])
-def test_q4_residual_forced_split_counts(monkeypatch, splits):
-    monkeypatch.setenv("GQA_ATTN_SPLITS", splits)
+def test_q4_residual_forced_split_counts(splits):
     n_quant, kv_lens = [4096, 1500, 0], [4096 + 100, 1500, 77]
     q, cache, kr, vr = make(3, 32, 8, 128, 4096, 128, n_quant, kv_lens, 9)
-    run_check(q, cache, kr, vr, n_quant, kv_lens)
+    with binding.plan_override(decode_splits=int(splits)):
+        run_check(q, cache, kr, vr, n_quant, kv_lens)
 
 
 def test_q4_residual_empty_request_is_zero_and_flagged():

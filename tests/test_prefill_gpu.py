@@ -120,14 +120,14 @@ def test_growing_scores_force_rescales(causal):
 @pytest.mark.parametrize("ks", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("q_len,kv_len,causal", [(1100, 1100, True), (200, 3000, True), (300, 2000, False),
                                                   (129, 300, True)])
-def test_kv_split_over_cluster(monkeypatch, ks, q_len, kv_len, causal):
+def test_kv_split_over_cluster(ks, q_len, kv_len, causal):
     """The KV range of each query-tile pair split over a cluster of ks CTAs
     (forced through the tuning override), partials merged through
     distributed shared memory; shares may be empty when ks exceeds the
     pair's KV tiles (129 queries at 300 keys: 3 tiles)."""
-    monkeypatch.setenv("GQA_ATTN_PREFILL_KSPLIT", str(ks))
     q, k, v = case(1, 14, 2, q_len, kv_len, layer=ks)
-    check_full(q, k, v, kv_len, causal)
+    with binding.plan_override(prefill_kv_split=ks):
+        check_full(q, k, v, kv_len, causal)
 
 
 @pytest.mark.parametrize("q_len,kv_len", [(300, 300), (512, 4096)])

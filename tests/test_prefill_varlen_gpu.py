@@ -63,9 +63,9 @@ def test_varlen_mix_matches_oracle(causal):
 
 
 @pytest.mark.parametrize("ks", ["1", "2", "3", "4", "5"])
-def test_varlen_under_forced_kv_splits(monkeypatch, ks):
-    monkeypatch.setenv("GQA_ATTN_PREFILL_KSPLIT", ks)
-    run_varlen([200, 33, 512], [3000, 700, 512], seed=2)
+def test_varlen_under_forced_kv_splits(ks):
+    with binding.plan_override(prefill_kv_split=int(ks)):
+        run_varlen([200, 33, 512], [3000, 700, 512], seed=2)
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(14, 2), (8, 8), (16, 2)])
@@ -85,3 +85,31 @@ def test_varlen_uniform_equals_plain_prefill():
     binding.gqa_attn_prefill_varlen(q, k, v, o2, lens(q_len), lens(kv_len), 0.125)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def test_prefill_status_word_flags_clamped_lengths():
+    """In-range lengths leave the prefill status word at 0; a key length past
+    S_cap or a query length past the request's keys is clamped and flagged."""
+    binding.gqa_attn_clear_prefill_status()
+    run_varlen(*MIX, seed=4)
+    assert binding.gqa_attn_read_prefill_status() == 0
+    B, S_cap, Tq_cap = 3, 256, 128
+    q = inputs.randn((B, 14, Tq_cap, 64), 11, torch.bfloat16, DEV)
+    k = inputs.randn((B, 2, S_cap, 64), 12, torch.bfloat16, DEV)
+    v = inputs.randn((B, 2, S_cap, 64), 13, torch.bfloat16, DEV)
+    o = torch.full_like(q, 3.0)
+    ql = torch.tensor([100, 128, 64], dtype=torch.int32, device=DEV)
+    kl = torch.tensor([256, 999, 20], dtype=torch.int32, device=DEV)  # 999 > S_cap; 64 queries > 20 keys
+    binding.gqa_attn_prefill_varlen(q, k, v, o, ql, kl, 0.125)
+    status = binding.gqa_attn_read_prefill_status()
+    assert status & binding.GQA_DEV_KVLEN_CLAMPED
+    assert not status & binding.GQA_DEV_WAIT_TIMEOUT
+    # the clamped requests computed what the clamped lengths define
+    got = f64(o)
+    for b, (qn, kn) in enumerate([(100, 256), (128, 256), (20, 20)]):
+        ref = oracle.attention(f64(q[b:b + 1, :, :qn]), f64(k[b:b + 1, :, :kn]), f64(v[b:b + 1, :, :kn]),
+                               scale=0.125, causal=True)["o"]
+        assert np.abs(got[b:b + 1, :, :qn] - ref).max() <= TOL
+    assert (got[2, :, 20:] == 3.0).all()
+    binding.gqa_attn_clear_prefill_status()
+    assert binding.gqa_attn_read_prefill_status() == 0
