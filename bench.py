@@ -159,9 +159,10 @@ def kernel_source_hash(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel_file, key):
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
-    source is unchanged since it was captured (else None)."""
+def recorded_ncu(kernel_file, key):
+    """The committed ncu record of one kernel (DRAM bytes and duration per
+    launch), if the kernel source is unchanged since it was captured (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -170,7 +171,13 @@ def recorded_traffic(kernel_file, key):
         return None
     if rec.get("source_sha256_16") != kernel_source_hash(kernel_file):
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec
+
+
+def recorded_traffic(kernel_file, key):
+    """Per-launch DRAM bytes from the committed ncu summary (or None)."""
+    rec = recorded_ncu(kernel_file, key)
+    return None if rec is None else rec.get("dram_bytes_per_launch")
 
 
 # ----------------------------------------------------------------------------- decode workload
@@ -585,26 +592,66 @@ def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iter
 
 ORACLE_SAMPLE = ("one KV head group (7 query heads, 1 of 4) of one layer call at kv_len=32768, "
                  "fp32 inputs widened to fp64; GB/s scaled by that sample's algorithmic bytes")
+ORACLE_SAMPLES = {
+    "decode": ORACLE_SAMPLE,
+    "prefill": ("causal prefill at Qwen2.5-0.5B head geometry, T=16384, bf16 inputs widened to fp64: "
+                "the last 128 query rows of one query head (each sees about 16,300 keys); "
+                "TFLOP/s from that sample's visible (query, key) pairs, 4*D flops each"),
+    "q4": ("4-bit decode at Qwen3-4B head geometry, kv_len=16384: one request's KV head group "
+           "(4 query heads, 1 of 8 heads x 4 requests), codes dequantised in fp64 then attended; "
+           "GB/s scaled by that sample's algorithmic bytes (codes, scales, biases, q, o)"),
+}
+PF_T, PF_ROWS = 16384, 128
+Q4_S = 16384
 
 
-def _oracle_sample_worker(n_steps, seed_layer, start, conn):
-    # one spawned process per host core, single-threaded BLAS (set by the parent)
-    import numpy as _np
+def _oracle_sample(kind, seed_layer):
+    """Inputs of one oracle sample and a function that runs it."""
     import oracle as _oracle
     from gqa_attention_kv_decode_gb300 import inputs as _inputs
     import torch as _torch
-    q, k, v = _inputs.qkv(1, HQ, HKV, D, 1, S_HEAD, _torch.float32, layer=seed_layer)
-    qs = q[:, 0:7].numpy()
-    ks = k[:, 0:1].numpy()
-    vs = v[:, 0:1].numpy()
-    conn.send("ready")
-    start.wait()
-    times = []
-    for _ in range(n_steps):
-        t0 = time.perf_counter()
-        _oracle.attention(qs, ks, vs, scale=D ** -0.5)
-        times.append(time.perf_counter() - t0)
-    conn.send(times)
+    if kind == "decode":
+        q, k, v = _inputs.qkv(1, HQ, HKV, D, 1, S_HEAD, _torch.float32, layer=seed_layer)
+        qs, ks, vs = q[:, 0:7].numpy(), k[:, 0:1].numpy(), v[:, 0:1].numpy()
+        return lambda: _oracle.attention(qs, ks, vs, scale=D ** -0.5)
+    if kind == "prefill":
+        q, k, v = _inputs.qkv(1, 14, 2, 64, PF_T, PF_T, _torch.bfloat16, layer=seed_layer)
+        qs = q[:, 0:1, PF_T - PF_ROWS:].float().numpy()
+        ks, vs = k[:, 0:1].float().numpy(), v[:, 0:1].float().numpy()
+        return lambda: _oracle.attention(qs, ks, vs, scale=0.125, causal=True)
+    if kind == "q4":
+        kc, ksc, kb, vc, vsc, vb = _inputs.q4_cache(1, 8, 128, Q4_S, layer=seed_layer)
+        q = _inputs.randn((1, 32, 1, 128), _inputs.tensor_seed(seed_layer, 0), _torch.bfloat16)
+        qs = q[:, 0:4].float().numpy()
+        cache = [t[:, 0:1].contiguous().numpy() for t in (kc, ksc, kb, vc, vsc, vb)]
+        return lambda: _oracle.attention_q4(qs, *cache, scale=128 ** -0.5)
+    raise ValueError(kind)
+
+
+def oracle_sample_units(kind):
+    """Algorithmic bytes (decode, q4) or flops (prefill) of one sample."""
+    if kind == "decode":
+        return 2 * 1 * S_HEAD * D * 4 + 2 * 7 * D * 4
+    if kind == "prefill":
+        pairs = sum(PF_T - PF_ROWS + i + 1 for i in range(PF_ROWS))
+        return 4 * 64 * pairs
+    if kind == "q4":
+        return Q4_S * (64 + 4 + 4) * 2 + 2 * 4 * 128 * 2
+    raise ValueError(kind)
+
+
+def _oracle_sample_worker(kinds, n_steps, seed_layer, starts, conn):
+    # one spawned process per host core, single-threaded BLAS (set by the parent)
+    for kind in kinds:
+        run = _oracle_sample(kind, seed_layer)
+        conn.send("ready")
+        starts[kind].wait()
+        times = []
+        for _ in range(n_steps):
+            t0 = time.perf_counter()
+            run()
+            times.append(time.perf_counter() - t0)
+        conn.send(times)
     conn.close()
 
 
@@ -612,29 +659,32 @@ def host_cores():
     return len(os.sched_getaffinity(0))
 
 
-def cpu_oracle_times(n_steps, workers=1):
+def cpu_oracle_times(n_steps, workers=1, kinds=("decode",)):
     """Per-step wall time of `workers` oracle processes (one per core, each on
-    its own layer's sample, single-threaded, started together): step i takes
-    the slowest worker's i-th sample."""
+    its own layer's sample, single-threaded, started together), per kind of
+    sample: step i takes the slowest worker's i-th sample."""
     import multiprocessing as mp
     env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
     saved = {k: os.environ.get(k) for k in env_keys}
     for k in env_keys:
         os.environ[k] = "1"
+    out = {}
     try:
         ctx = mp.get_context("spawn")
-        start = ctx.Event()
+        starts = {kind: ctx.Event() for kind in kinds}
         procs, pipes = [], []
         for w in range(workers):
             parent, child = ctx.Pipe()
-            p = ctx.Process(target=_oracle_sample_worker, args=(n_steps, w, start, child))
+            p = ctx.Process(target=_oracle_sample_worker, args=(tuple(kinds), n_steps, w, starts, child))
             p.start()
             procs.append(p)
             pipes.append(parent)
-        for parent in pipes:
-            assert parent.recv() == "ready"
-        start.set()
-        per_worker = [parent.recv() for parent in pipes]
+        for kind in kinds:
+            for parent in pipes:
+                assert parent.recv() == "ready"
+            starts[kind].set()
+            per_worker = [parent.recv() for parent in pipes]
+            out[kind] = [max(ts[i] for ts in per_worker) for i in range(n_steps)]
         for p in procs:
             p.join()
     finally:
@@ -643,25 +693,40 @@ def cpu_oracle_times(n_steps, workers=1):
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = val
-    return [max(ts[i] for ts in per_worker) for i in range(n_steps)]
+    return out
 
 
 def oracle_sample_bytes():
-    return 2 * 1 * S_HEAD * D * 4 + 2 * 7 * D * 4
+    return oracle_sample_units("decode")
+
+
+def _oracle_rate(kind, cores, seconds):
+    units = cores * oracle_sample_units(kind) / seconds
+    return units / 1e12 if kind == "prefill" else units / 1e9
 
 
 def cpu_baseline(n_steps=3):
     """The oracle on every host core this process may use (one sample per
-    core, run together), and on one core."""
+    core, run together), and on one core: the headline decode sample, and
+    beside it a causal-prefill and a 4-bit-decode sample."""
     cores = host_cores()
-    t = statistics.median(cpu_oracle_times(n_steps, cores))
-    t1 = statistics.median(cpu_oracle_times(n_steps, 1))
-    return {"value": round(cores * oracle_sample_bytes() / t / 1e9, 3), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
-            "sample": ORACLE_SAMPLE + f"; {cores} samples (one per core, distinct layers) at once, median of {n_steps}",
-            "seconds_per_sample": round(t, 3),
-            "single_core": {"value": round(oracle_sample_bytes() / t1 / 1e9, 3), "cores": 1,
-                            "seconds_per_sample": round(t1, 3)}}
+    kinds = ("decode", "prefill", "q4")
+    many = cpu_oracle_times(n_steps, cores, kinds)
+    one = cpu_oracle_times(n_steps, 1, kinds)
+    res = {}
+    for kind in kinds:
+        t, t1 = statistics.median(many[kind]), statistics.median(one[kind])
+        res[kind] = {"value": round(_oracle_rate(kind, cores, t), 4),
+                     "unit": "TFLOP/s" if kind == "prefill" else "GB/s", "cores": cores, "kind": "oracle",
+                     "sample": ORACLE_SAMPLES[kind] + f"; {cores} samples (one per core, distinct layers) at "
+                                                      f"once, median of {n_steps}",
+                     "seconds_per_sample": round(t, 4),
+                     "single_core": {"value": round(_oracle_rate(kind, 1, t1), 4), "cores": 1,
+                                     "seconds_per_sample": round(t1, 4)}}
+    base = dict(res["decode"])
+    base["prefill_T16384"] = res["prefill"]
+    base["q4_decode_S16384"] = res["q4"]
+    return base
 
 
 def run_reference(args):
@@ -669,7 +734,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     cores = host_cores()
-    times = cpu_oracle_times(args.warmup + args.steps, cores)[args.warmup:]
+    times = cpu_oracle_times(args.warmup + args.steps, cores)["decode"][args.warmup:]
     t = sum(times) / len(times)
     value = cores * oracle_sample_bytes() / t / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
@@ -961,6 +1026,13 @@ def main():
     del host, host_out
 
     traffic = recorded_traffic("decode.cu", "decode_f32_d128_nrep7_S32768")
+    # the split kernel alone, as ncu timed it (cold, serialised, no overlap)
+    rec = recorded_ncu("decode.cu", "decode_f32_d128_nrep7_S32768")
+    isolated_kernel_frac = None
+    if rec and rec.get("ncu_duration_ns"):
+        isolated_kernel_frac = {"value": round(per_launch_bytes / (rec["ncu_duration_ns"] * 1e-9) / 1e9 / hbm_peak, 4),
+                                "kernel_us": rec["ncu_duration_ns"] / 1e3,
+                                "source": "profiles/traffic.json (ncu gpu__time_duration.sum of the split kernel)"}
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -984,6 +1056,9 @@ def main():
                      "peak_source": peak_src, "avg_launch_us": round(avg_launch_us, 3),
                      "timing": "events on the launching stream around the K timed steps / (K x 28 calls)",
                      "isolated_call_us": round(isolated_call_us, 3),
+                     "basis": "per-call stream average: consecutive calls overlap (each split kernel "
+                              "is launched early and prefetches into L2 while the previous merge runs)",
+                     "isolated_kernel_frac": isolated_kernel_frac,
                      "n_split": n_split},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
@@ -1006,6 +1081,8 @@ def main():
                                                    for B in (1, 2, 4, 8, 16, 64)]
         line["q4_decode_qwen3_4b_B4_36_layers"] = [q4_point(binding, S, device, stream, flush)
                                                   for S in (64, 2048, 16384)]
+        if cpu is not None:  # the oracle beside the GPU figure, same metric
+            line["q4_decode_qwen3_4b_B4_36_layers"][-1]["cpu_oracle"] = cpu["q4_decode_S16384"]
         line["paged_decode_qwen3_4b_36_layers"] = [paged_point(binding, B, device, stream, flush)
                                                    for B in (16, 64)]
         line["quantize_q4_qwen3_4b"] = quantize_point(binding, device, stream, flush)
@@ -1017,6 +1094,8 @@ def main():
                                                      for B in (4, 16)]
         pf = [prefill_point(binding, T, T, device, stream, flush, bf16_peak) for T in (513, 2049, 4097, 16384)]
         pf.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak))
+        if cpu is not None:
+            pf[3]["cpu_oracle"] = cpu["prefill_T16384"]
         line["prefill_causal_qwen05b_bf16"] = pf
         big = pf[3]
         line["roofline_prefill"] = {"bound": "tensor", "achieved": big["TFLOPs"], "peak": bf16_peak,
