@@ -1,7 +1,8 @@
 """Split-KV decode on the GPU against the fp64 oracle, element by element.
 
-Tolerances (max abs error): 1e-4 for fp32 Q/K/V/O, 2e-2 for bf16 with fp32
-accumulation.  Lengths, head mapping and tails must be exact: rows past
+Bounds (tests/parity.py): max abs error 1e-4 for fp32 Q/K/V/O and 2e-2 for
+bf16 with fp32 accumulation, and per output row an error scaled to the
+row's largest reference value (2^-16 fp32, 2^-6 bf16).  Lengths, head mapping and tails must be exact: rows past
 kv_len are filled with NaN, so a kernel that reads them (instead of skipping
 them) fails.
 """
@@ -13,11 +14,11 @@ import pytest
 import torch
 
 import oracle
+import parity
 from gqa_attention_kv_decode_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
 
-TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
 DEV = "cuda"
 
 
@@ -42,11 +43,7 @@ def check(q, k, v, o, kv_lens=None, scale=None):
     D = q.shape[-1]
     scale = D ** -0.5 if scale is None else scale
     ref = oracle.attention(f64(q), f64(k), f64(v), kv_lens=kv_lens, scale=scale)["o"]
-    got = f64(o)
-    assert np.isfinite(got).all()
-    err = float(np.abs(got - ref).max())
-    assert err <= TOL[q.dtype], f"max abs err {err}"
-    return err
+    return parity.check(f64(o), ref, parity.kind_of(q.dtype))
 
 
 HEADS = [(14, 2), (28, 4), (32, 8), (8, 8), (6, 3), (12, 4), (10, 2), (16, 2), (24, 2), (32, 2)]
@@ -105,7 +102,7 @@ def test_empty_and_out_of_range_lengths_set_status():
     got = f64(o)
     assert (got[0] == 0).all() and (got[3] == 0).all()     # 0 and -3 -> empty
     ref = oracle.attention(f64(q), f64(k), f64(v), kv_lens=[0, 100, 100, 0], scale=D ** -0.5)["o"]
-    assert np.abs(got - ref).max() <= 1e-4                  # 150 clamped to max_kv_len
+    parity.check(got, ref, "f32", "150 clamped to max_kv_len")
     binding.gqa_attn_clear_device_status(ws)
     assert binding.gqa_attn_read_device_status(ws) == 0
 
@@ -156,13 +153,13 @@ def test_config_qwen7b_28_layers(dtype, S):
             hs = slice(7 * g, 7 * g + 7)
             ref = oracle.attention(f64(q[:, hs]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1]),
                                    scale=128 ** -0.5)["o"]
-            assert np.abs(f64(outs[l][:, hs]) - ref).max() <= TOL[dtype]
+            parity.check(f64(outs[l][:, hs]), ref, parity.kind_of(dtype), f"layer {l} group {g}")
 
 
 @pytest.mark.parametrize("B", [1, 2, 4, 8, 16, 64])
 def test_config_qwen3_4b_ragged_36_layers(B):
     """Hq=32, Hkv=8, D=128, bf16, lengths uniform in [64, 8192], 36 layers;
-    sampled (layer, request) pairs checked against the oracle."""
+    every request of four sampled layers checked against the oracle."""
     kv_lens = inputs.ragged_kv_lens(B, 64, 8192, seed=inputs.BASE_SEED + B)
     lens_t = torch.from_numpy(kv_lens).to(DEV)
     ws = binding.decode_workspace(B, 32, 8, 128, 8192, binding.GQA_BF16)
@@ -174,11 +171,11 @@ def test_config_qwen3_4b_ragged_36_layers(B):
         if l not in check_layers:
             continue
         torch.cuda.synchronize()
-        for b in rng.choice(B, min(B, 3), replace=False):
+        for b in range(B):
             L = int(kv_lens[b])
             ref = oracle.attention(f64(q[b:b + 1]), f64(k[b:b + 1, :, :L]), f64(v[b:b + 1, :, :L]),
                                    scale=128 ** -0.5)["o"]
-            assert np.abs(f64(o[b:b + 1]) - ref).max() <= 2e-2
+            parity.check(f64(o[b:b + 1]), ref, "bf16", f"layer {l} request {b}")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -194,5 +191,4 @@ def test_back_to_back_calls_read_the_previous_output(dtype):
     o2 = binding.decode(o1, k2, v2, workspace=ws)
     torch.cuda.synchronize()
     ref2 = oracle.attention(f64(o1), f64(k2), f64(v2), scale=128 ** -0.5)["o"]
-    err = np.abs(f64(o2) - ref2).max()
-    assert err <= TOL[dtype], f"max abs err {err}"
+    parity.check(f64(o2), ref2, parity.kind_of(dtype))

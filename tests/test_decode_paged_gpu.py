@@ -4,7 +4,7 @@ the fp64 oracle.
 The pools hold every request's blocks in a seeded random order, spare blocks
 and every row past kv_len are NaN, and the appended token's slot starts as
 NaN: a kernel that reads a row it should not, or misses the append, fails.
-Tolerances as for contiguous decode (max abs error 1e-4 fp32, 2e-2 bf16); the
+Bounds as for contiguous decode (tests/parity.py: absolute and row-scaled); the
 pool rows written by the append must equal the new token bit for bit.
 """
 
@@ -13,11 +13,11 @@ import pytest
 import torch
 
 import oracle
+import parity
 from gqa_attention_kv_decode_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,9 +53,7 @@ def run_and_check(q, kp, vp, table, kn, vn, kv_lens, max_kv_len, block_size):
     o = binding.decode_paged(q, kp, vp, table, lens_t, max_kv_len, k_new=kn, v_new=vn)
     torch.cuda.synchronize()
     got = f64(o)
-    assert np.isfinite(got).all()
-    err = float(np.abs(got - ref["o"]).max())
-    assert err <= TOL[q.dtype], f"max abs err {err}"
+    parity.check(got, ref["o"], parity.kind_of(q.dtype))
     if kn is not None:  # the pools now hold the new tokens at row kv_len - 1
         for b, L in enumerate(kv_lens):
             if L == 0:
@@ -109,7 +107,7 @@ def test_paged_bad_block_id_is_reported_and_stays_in_the_pool():
     assert status & binding.GQA_DEV_BAD_BLOCK
     ref = oracle.attention_paged(f64(q[1:]), f64(kp), f64(vp), table[1:].cpu().numpy(), kv_lens[1:], 64,
                                  scale=128 ** -0.5)
-    assert np.abs(f64(o[1:]) - ref["o"]).max() <= TOL[torch.bfloat16]  # the other request is intact
+    parity.check(f64(o[1:]), ref["o"], "bf16", "the other request is intact")
 
 
 def test_paged_rejects_unsupported_block_size():

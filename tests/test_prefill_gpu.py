@@ -1,10 +1,10 @@
 """Causal / chunked prefill on the tcgen05 tensor cores against the oracle.
 
-bf16 Q/K/V/O, fp32 accumulation; tolerance max abs error 2e-2.  The causal
+bf16 Q/K/V/O, fp32 accumulation; bounds (tests/parity.py) max abs error 2e-2
+and, per output row, 2^-6 of its largest reference value.  The causal
 mask is aligned to the end of the keys: with q_len < kv_len (a chunk), query
 row i sees keys j <= i + kv_len - q_len.  For the 16,384-token case the
-oracle checks sampled rows one at a time (row i of a full causal prefill is
-a single query over keys 0..i).
+oracle checks every row of two query heads, 2048 rows at a time.
 """
 
 import numpy as np
@@ -12,11 +12,11 @@ import pytest
 import torch
 
 import oracle
+import parity
 from gqa_attention_kv_decode_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL = 2e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,10 +41,7 @@ def check_full(q, k, v, kv_len, causal):
     torch.cuda.synchronize()
     ref = oracle.attention(f64(q), f64(k[:, :, :kv_len]), f64(v[:, :, :kv_len]),
                            scale=0.125, causal=causal)["o"]
-    got = f64(o)
-    assert np.isfinite(got).all()
-    err = np.abs(got - ref).max()
-    assert err <= TOL, f"max abs err {err}"
+    parity.check(f64(o), ref, "bf16")
 
 
 @pytest.mark.parametrize("T", [1, 5, 127, 128, 129, 300, 513])
@@ -92,17 +89,22 @@ def test_config_chunked_prefill_512_at_3584():
     check_full(q, k, v, 4096, True)
 
 
-def test_config_causal_prefill_16384_sampled_rows():
+def test_config_causal_prefill_16384_two_heads_every_row():
+    """Every row of query heads 0 and 13 (KV heads 0 and 1).  Rows [r0, r1)
+    of a causal prefill are a chunk of r1 - r0 queries aligned to the end of
+    keys [0, r1), so the oracle runs in chunks of 2048 rows."""
     T = 16384
     q, k, v = case(1, 14, 2, T, T, layer=3)
     o = binding.prefill(q, k, v, causal=True)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(T)
-    rows = sorted(set([0, 1, 127, 128, 8191, T - 1] + list(rng.integers(0, T, 10))))
-    qn, kn, vn, on = f64(q), f64(k), f64(v), f64(o)
-    for i in rows:
-        ref = oracle.attention(qn[:, :, i:i + 1], kn[:, :, :i + 1], vn[:, :, :i + 1], scale=0.125)["o"]
-        assert np.abs(on[:, :, i:i + 1] - ref).max() <= TOL, f"row {i}"
+    on = f64(o)
+    for h in (0, 13):
+        g = h // 7
+        qh, kh, vh = f64(q[:, h:h + 1]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1])
+        for r0 in range(0, T, 2048):
+            r1 = r0 + 2048
+            ref = oracle.attention(qh[:, :, r0:r1], kh[:, :, :r1], vh[:, :, :r1], scale=0.125, causal=True)["o"]
+            parity.check(on[:, h:h + 1, r0:r1], ref, "bf16", f"head {h} rows {r0}..{r1}")
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -142,7 +144,6 @@ def test_back_to_back_calls_read_the_previous_output(q_len, kv_len):
     o2 = binding.prefill(o1, k2, v2)
     torch.cuda.synchronize()
     ref1 = oracle.attention(f64(q), f64(k), f64(v), scale=0.125, causal=True)["o"]
-    assert np.abs(f64(o1) - ref1).max() <= TOL
+    parity.check(f64(o1), ref1, "bf16", "first call")
     ref2 = oracle.attention(f64(o1), f64(k2), f64(v2), scale=0.125, causal=True)["o"]
-    err = np.abs(f64(o2) - ref2).max()
-    assert err <= TOL, f"max abs err {err}"
+    parity.check(f64(o2), ref2, "bf16", "second call")
