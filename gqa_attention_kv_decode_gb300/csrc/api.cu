@@ -67,6 +67,12 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   return p;
 }
 
+SplitPlan decode_plan(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype, bool paged) {
+  const long units = long(B) * Hkv * ((Hq / Hkv + 7) / 8);
+  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D, paged, units, max_kv_len),
+                     device_sm_count(), decode_ctas_per_sm(dtype, paged, units, max_kv_len));
+}
+
 }  // namespace gqa
 
 using namespace gqa;
@@ -163,15 +169,20 @@ GQA_ATTN_API size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int D
                                                    int dtype) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return 0;
-  return decode_ws_size(B, Hq, Hkv, D, max_kv_len, decode_tile_rows(dtype, D), decode_ctas_per_sm(dtype));
+  // the same workspace serves gqa_attn_decode_paged, whose kernel may plan
+  // more splits: the larger of the two plans
+  const SplitPlan c = decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, false);
+  const SplitPlan pg = decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, true);
+  const size_t contiguous = workspace_layout(B, Hq, Hkv, c.n_hc, c.n_split, D).total;
+  const size_t paged = workspace_layout(B, Hq, Hkv, pg.n_hc, pg.n_split, D).total;
+  return contiguous > paged ? contiguous : paged;
 }
 
 GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
                                             int dtype) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return GQA_ERR_INVALID_ARG;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
-  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
-                     decode_ctas_per_sm(dtype)).n_split;
+  return decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, false).n_split;
 }
 
 GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, void* o,
@@ -202,8 +213,7 @@ GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, vo
   a.scale = scale;
   a.dtype = dtype;
   a.workspace = workspace;
-  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
-                       decode_ctas_per_sm(dtype));
+  a.plan = decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, false);
   if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
     return GQA_ERR_WORKSPACE;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
@@ -215,8 +225,7 @@ GQA_ATTN_API size_t gqa_attn_decode_layers_workspace_size(int n_layers, int B, i
   if (n_layers < 1 || long(n_layers) * B > 65535) return 0;
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return 0;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return 0;
-  const SplitPlan p = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
-                                  decode_ctas_per_sm(dtype));
+  const SplitPlan p = decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, false);
   return workspace_layout(n_layers * B, Hq, Hkv, p.n_hc, p.n_split, D).total;
 }
 
@@ -258,8 +267,7 @@ GQA_ATTN_API int gqa_attn_decode_layers(const void* q, const void* k, const void
   a.kv_period = B;
   // the single-layer plan: every (layer, request, head, split) CTA does the
   // work it does in a one-layer call, so the results are bit-identical
-  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
-                       decode_ctas_per_sm(dtype));
+  a.plan = decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, false);
   if (ws_bytes < workspace_layout(a.B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total) return GQA_ERR_WORKSPACE;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
   return GQA_OK;
@@ -276,7 +284,7 @@ GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const v
   int rc = check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, scale);
   if (rc != GQA_OK) return rc;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
-  if (block_size % decode_tile_rows(dtype, D) != 0) return GQA_ERR_UNSUPPORTED;
+  if (block_size % decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, true).tile != 0) return GQA_ERR_UNSUPPORTED;
   // block ids index [num_blocks * Hkv] (block, head) slabs of block_size rows
   if (long(num_blocks) * Hkv > 0x7fffffffL || long(num_blocks) * Hkv * block_size > 0x7fffffffL)
     return GQA_ERR_INVALID_ARG;
@@ -317,8 +325,7 @@ GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const v
   a.num_blocks = num_blocks;
   a.k_new = k_new;
   a.v_new = v_new;
-  a.plan = plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D), device_sm_count(),
-                       decode_ctas_per_sm(dtype));
+  a.plan = decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, true);
   if (ws_bytes < workspace_layout(B, Hq, Hkv, a.plan.n_hc, a.plan.n_split, D).total)
     return GQA_ERR_WORKSPACE;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
@@ -450,7 +457,7 @@ GQA_ATTN_API int gqa_attn_decode_q4_residual(
   ar.dtype = GQA_BF16;
   ar.workspace = workspace;
   ar.plan = aq.plan;
-  ar.plan.tile = decode_tile_rows(GQA_BF16, D);
+  ar.plan.tile = decode_tile_rows(GQA_BF16, D, false, long(B) * Hkv * aq.plan.n_hc, R_cap);
   ar.plan.chunk = ((R_cap + ar.plan.tile - 1) / ar.plan.tile) * ar.plan.tile;
   ar.plan.n_split = 1;
   const cudaError_t e = launch_decode_q4_residual(aq, ar, static_cast<cudaStream_t>(stream));

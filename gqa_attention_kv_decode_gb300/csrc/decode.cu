@@ -565,13 +565,15 @@ cudaError_t dispatch_nrep(const DecodeParams& p, dim3 grid, cudaStream_t s) {
 
 }  // namespace
 
-// bf16 caches run on the tensor cores (decode_mma.cu), in tiles of 64 keys,
-// two CTAs per SM.
-int decode_ctas_per_sm(int dtype) { return dtype == GQA_F32 ? 1 : 2; }
+// bf16 caches run on the tensor cores (decode_mma.cu), whose kernel shape
+// (tile height, CTAs per SM) depends on the problem.
+int decode_ctas_per_sm(int dtype, bool paged, long units, int max_kv_len) {
+  return dtype == GQA_F32 ? 1 : decode_mma_ctas_per_sm(paged, units, max_kv_len);
+}
 
-int decode_tile_rows(int dtype, int D) {
+int decode_tile_rows(int dtype, int D, bool paged, long units, int max_kv_len) {
   if (dtype == GQA_F32) return D == 128 ? TileCfg<float, 128>::TILE : TileCfg<float, 64>::TILE;
-  return 64;
+  return decode_mma_tile_rows(paged, units, max_kv_len);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {

@@ -66,13 +66,27 @@ struct MmaParams {
   int kv_period;      // > 0: layers stacked along the batch axis share kv_lens[b % kv_period]
 };
 
-template <int D, int NSTAGE>
+// Two shapes of the contiguous-cache kernel.  For long contexts with few
+// (request, KV head) units -- a single long request -- 8 warps per CTA, one
+// CTA per SM, tiles of 128 keys: half the split partials for the merge to
+// read and twice the keys per split (7B geometry, 32K keys: 15.25 -> 14.7 us
+// per call).  Otherwise two 4-warp CTAs per SM with tiles of 64 keys: more
+// CTAs to spread a short context over (a single SM streams only about
+// 40 GB/s, so short contexts need many SMs), and with many units, multi-wave
+// grids whose two CTAs per SM overlap each other's ramps and tails (Qwen3-4B
+// ragged B = 4..64: the 8-warp shape was 18-20 % slower; 7B geometry at 2K
+// keys: 7.1 against 5.7 us per call).
+constexpr int kWideUnits = 16;      // units up to which the 8-warp shape may be used
+constexpr int kWideMinKeys = 8192;  // and keys from which it is used
+
+template <int D, int NSTAGE, int NW_>
 struct MmaCfg {
-  static constexpr int TILE = 64;             // keys per tile
-  static constexpr int NW = 4;                // warps; warp w takes keys [16w, 16w + 16)
+  static constexpr int NW = NW_;              // warps; warp w takes keys [16w, 16w + 16)
+  static constexpr int TILE = 16 * NW;        // keys per tile
   static constexpr int NTHR = 32 * NW;
-  static constexpr int HALVES = D / 64;       // 128-byte TMA boxes per key row
-  static constexpr int BOX = TILE * 128;      // one box: 64 rows x 128 bytes
+  static constexpr int HALVES = D / 64;       // 128-byte columns per key row
+  static constexpr int BOX = TILE * 128;      // one column of the tile: TILE rows x 128 bytes
+  static constexpr int SUB = TILE / 64;       // TMA boxes (64 rows x 128 bytes) per column
   static constexpr int TILEB = HALVES * BOX;  // K (or V) tile
   static constexpr int STAGEB = 2 * TILEB;    // K + V
   static constexpr int OFF_BAR = NSTAGE * STAGEB;
@@ -120,11 +134,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // PAGED: K and V tiles come from block pools through the block table (a tile
 // never crosses a block); with k_new the CTA that owns row kv_len - 1 writes
 // the new token into its tile in shared memory and into the pool.
-template <int D, int NSTAGE, bool PAGED>
-__global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
+template <int D, int NSTAGE, int NW, bool PAGED>
+__global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const MmaParams p) {
-  using C = MmaCfg<D, NSTAGE>;
+  using C = MmaCfg<D, NSTAGE, NW>;
   constexpr int TILE = C::TILE;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -220,10 +234,14 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE>::NTHR, 2)
     mbar_arrive_expect_tx(&full[st], C::STAGEB);
 #pragma unroll
     for (int hf = 0; hf < C::HALVES; ++hf)
-      tma_load_3d(dst + hf * C::BOX, &tmK, hf * 64, mrow, mhead, &full[st]);
+#pragma unroll
+      for (int sb = 0; sb < C::SUB; ++sb)
+        tma_load_3d(dst + hf * C::BOX + sb * 8192, &tmK, hf * 64, mrow + sb * 64, mhead, &full[st]);
 #pragma unroll
     for (int hf = 0; hf < C::HALVES; ++hf)
-      tma_load_3d(dst + C::TILEB + hf * C::BOX, &tmV, hf * 64, mrow, mhead, &full[st]);
+#pragma unroll
+      for (int sb = 0; sb < C::SUB; ++sb)
+        tma_load_3d(dst + C::TILEB + hf * C::BOX + sb * 8192, &tmV, hf * 64, mrow + sb * 64, mhead, &full[st]);
   };
   // The appended token (row L - 1) lies in tile (L - 1) / TILE, which is
   // tile t_new of split ((L - 1) / TILE) % n_used.
@@ -453,11 +471,11 @@ bool kv_map(CUtensorMap* out, const void* base, int D, int S_cap, int heads) {
   return true;
 }
 
-template <int D, int NSTAGE, bool PAGED>
+template <int D, int NSTAGE, int NW, bool PAGED>
 cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& p, dim3 grid,
                        cudaStream_t stream) {
-  using C = MmaCfg<D, NSTAGE>;
-  auto kern = decode_mma_kernel<D, NSTAGE, PAGED>;
+  using C = MmaCfg<D, NSTAGE, NW>;
+  auto kern = decode_mma_kernel<D, NSTAGE, NW, PAGED>;
   static std::once_flag once;
   static cudaError_t cfg_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -471,6 +489,19 @@ cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPa
 }
 
 }  // namespace
+
+// Tile height (16 keys per warp) and CTAs per SM of the kernel shape used for
+// `units` (request, KV head chunk) pairs and `max_kv_len` keys; the paged
+// kernel always has 4 warps, so that a 64-row block holds whole tiles.
+static bool wide_shape(bool paged, long units, int max_kv_len) {
+  return !paged && units <= kWideUnits && max_kv_len >= kWideMinKeys;
+}
+int decode_mma_tile_rows(bool paged, long units, int max_kv_len) {
+  return wide_shape(paged, units, max_kv_len) ? 128 : 64;
+}
+int decode_mma_ctas_per_sm(bool paged, long units, int max_kv_len) {
+  return wide_shape(paged, units, max_kv_len) ? 1 : 2;
+}
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   if (a.D != 64 && a.D != 128) return cudaErrorNotSupported;
@@ -519,8 +550,15 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.kv_period = a.kv_period;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   if (paged)
-    return a.D == 128 ? launch_mma<128, 3, true>(tk, tv, p, grid, stream) : launch_mma<64, 6, true>(tk, tv, p, grid, stream);
-  return a.D == 128 ? launch_mma<128, 3, false>(tk, tv, p, grid, stream) : launch_mma<64, 6, false>(tk, tv, p, grid, stream);
+    return a.D == 128 ? launch_mma<128, 3, 4, true>(tk, tv, p, grid, stream)
+                      : launch_mma<64, 6, 4, true>(tk, tv, p, grid, stream);
+  // the shape follows the plan's tile height
+  if (a.plan.tile == 128)
+    return a.D == 128 ? launch_mma<128, 3, 8, false>(tk, tv, p, grid, stream)
+                      : launch_mma<64, 6, 8, false>(tk, tv, p, grid, stream);
+  if (a.plan.tile != 64) return cudaErrorInvalidValue;
+  return a.D == 128 ? launch_mma<128, 3, 4, false>(tk, tv, p, grid, stream)
+                    : launch_mma<64, 6, 4, false>(tk, tv, p, grid, stream);
 }
 
 }  // namespace gqa

@@ -83,8 +83,13 @@ struct DecodeArgs {
 
 // Tile height (rows) of the decode kernel for this dtype / head size, and how
 // many of its CTAs an SM holds.
-int decode_tile_rows(int dtype, int D);
-int decode_ctas_per_sm(int dtype);
+// `units`: (request, KV head chunk) pairs of one call, B * Hkv * n_hc.
+int decode_tile_rows(int dtype, int D, bool paged, long units, int max_kv_len);
+int decode_ctas_per_sm(int dtype, bool paged, long units, int max_kv_len);
+int decode_mma_tile_rows(bool paged, long units, int max_kv_len);
+int decode_mma_ctas_per_sm(bool paged, long units, int max_kv_len);
+// The decode plan of one layer call (contiguous or paged cache).
+SplitPlan decode_plan(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype, bool paged);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);  // bf16 caches (tensor cores)
 

@@ -62,6 +62,20 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
   const int c4 = tid % D4, sg = tid / D4;
   grid_launch_dependents();  // the next call's split kernel may start staging
   grid_dependency_wait();
+  // The first PRE partials of every split group are loaded for all planned
+  // slots at once, together with the request's length, so that the two
+  // round trips overlap; slots past the request's splits are masked below.
+  const float2* ml = p.ml + size_t(bh) * p.n_split;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + size_t(bh) * p.n_split * D) + c4;
+  float4 x[PRE];
+  float2 mlv[PRE];
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int sidx = sg + k * NSG;
+    const bool in = sidx < p.n_split;
+    x[k] = in ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    mlv[k] = in ? __ldcg(&ml[sidx]) : make_float2(-INFINITY, 0.f);
+  }
   int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;
   int n_used;
   if (p.n_quant != nullptr) {
@@ -84,17 +98,12 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
     n_used = (L + p.chunk - 1) / p.chunk;
     if (n_used <= 1) return;  // written by the split kernel itself
   }
-  const float2* ml = p.ml + size_t(bh) * p.n_split;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + size_t(bh) * p.n_split * D) + c4;
-  float4 x[PRE];
-  float2 mlv[PRE];
 #pragma unroll
-  for (int k = 0; k < PRE; ++k) {
-    const int sidx = sg + k * NSG;
-    const bool in = sidx < n_used;
-    x[k] = in ? __ldcg(po + size_t(sidx) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    mlv[k] = in ? __ldcg(&ml[sidx]) : make_float2(-INFINITY, 0.f);
-  }
+  for (int k = 0; k < PRE; ++k)
+    if (sg + k * NSG >= n_used) {  // loaded above, but not a split of this request
+      x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      mlv[k] = make_float2(-INFINITY, 0.f);
+    }
   float M = -INFINITY;
 #pragma unroll
   for (int k = 0; k < PRE; ++k) M = fmaxf(M, mlv[k].x);

@@ -53,7 +53,7 @@ def run_and_check(q, kp, vp, table, kn, vn, kv_lens, max_kv_len, block_size):
     o = binding.decode_paged(q, kp, vp, table, lens_t, max_kv_len, k_new=kn, v_new=vn)
     torch.cuda.synchronize()
     got = f64(o)
-    parity.check(got, ref["o"], parity.kind_of(q.dtype))
+    err = parity.check(got, ref["o"], parity.kind_of(q.dtype))
     if kn is not None:  # the pools now hold the new tokens at row kv_len - 1
         for b, L in enumerate(kv_lens):
             if L == 0:
