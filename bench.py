@@ -546,8 +546,10 @@ def q4_point(binding, S, device, stream, flush, iters=10):
     return {"S": S, "us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
 
 
-def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iters=8, NL=PREFILL_LAYERS):
-    """Hq=14, Hkv=2, D=64, bf16, causal, queries aligned to the end of the keys.
+def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iters=8, NL=PREFILL_LAYERS,
+                  Hq=14, Hkv=2, D=64):
+    """bf16, causal, queries aligned to the end of the keys; head geometry
+    Hq=14, Hkv=2, D=64 (Qwen2.5-0.5B) unless given.
 
     One step is NL launches on NL distinct buffer sets (a prefill through the
     model's layers), timed with one event pair after an L2 flush: no launch
@@ -556,15 +558,15 @@ def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iter
     step time / NL (median over the steps)."""
     layers = []
     for l in range(NL):
-        q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(l, 0), torch.bfloat16, device)
-        k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(l, 1), torch.bfloat16, device)
-        v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(l, 2), torch.bfloat16, device)
+        q = inputs.randn((1, Hq, q_len, D), inputs.tensor_seed(l, 0), torch.bfloat16, device)
+        k = inputs.randn((1, Hkv, kv_len, D), inputs.tensor_seed(l, 1), torch.bfloat16, device)
+        v = inputs.randn((1, Hkv, kv_len, D), inputs.tensor_seed(l, 2), torch.bfloat16, device)
         layers.append((q, k, v, torch.empty_like(q)))
     torch.cuda.synchronize()
 
     def step():
         for q, k, v, o in layers:
-            binding.gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, stream)
+            binding.gqa_attn_prefill(q, k, v, o, kv_len, D ** -0.5, True, stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
             step()
@@ -580,12 +582,15 @@ def prefill_point(binding, q_len, kv_len, device, stream, flush, bf16_peak, iter
             evs.append((e0, e1))
     torch.cuda.synchronize()
     us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs) / NL
-    flops = metrics.prefill_flops(14, 64, q_len, kv_len, causal=True)
+    flops = metrics.prefill_flops(Hq, D, q_len, kv_len, causal=True)
     tf = flops / us / 1e6
     del layers
     torch.cuda.empty_cache()
-    return {"q_len": q_len, "kv_len": kv_len, "layers": NL, "us": round(us, 2), "TFLOPs": round(tf, 1),
-            "tokens_per_s": round(q_len / us * 1e6, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
+    row = {"q_len": q_len, "kv_len": kv_len, "layers": NL, "us": round(us, 2), "TFLOPs": round(tf, 1),
+           "tokens_per_s": round(q_len / us * 1e6, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
+    if (Hq, Hkv, D) != (14, 2, 64):
+        row = {"Hq": Hq, "Hkv": Hkv, "D": D, **row}
+    return row
 
 
 # ----------------------------------------------------------------------------- CPU oracle

@@ -477,7 +477,7 @@ GQA_ATTN_API int gqa_attn_prefill(const void* q, const void* k, const void* v, v
   if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return GQA_ERR_INVALID_ARG;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
-  if (dtype != GQA_BF16 || D != 64) return GQA_ERR_UNSUPPORTED;
+  if (dtype != GQA_BF16) return GQA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   const int rc = check_ptrs({q, k, v, o}, dev, 16);
@@ -513,7 +513,7 @@ GQA_ATTN_API int gqa_attn_prefill_varlen(const void* q, const void* k, const voi
   if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return GQA_ERR_INVALID_ARG;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
-  if (dtype != GQA_BF16 || D != 64) return GQA_ERR_UNSUPPORTED;
+  if (dtype != GQA_BF16) return GQA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   int rc = check_ptrs({q, k, v, o}, dev, 16);

@@ -2,23 +2,26 @@
 // sm_103a ("Fused attention makes a 4,096-token Qwen2 prefill on Metal 4.5x
 // faster", "Cause and workaround": one pass over the grouped KV heads, the
 // causal mask applied inside the kernel with the queries aligned to the end
-// of the keys, no score matrix in memory).
+// of the keys, no score matrix in memory).  Head dimension 64 or 128.
 //
 // One CTA computes two consecutive 128-row query tiles (A and B) of one query
 // head h and reads KV head g = h / n_rep directly (no repeat_kv).  Roles:
 //   warpgroup 2, warp 8   TMA: Q_A, Q_B once, then K and V tiles of 128 keys
-//                         through 4 shared-memory stages;
-//   warpgroup 2, warp 9   MMA issue of S_t = Q_t K^T (M=128, N=128, K=64);
-//   warps 10, 11          MMA issue of O_t += P_t V (M=128, N=64, K=128) for
-//                         t = A, B; S, P and O live in tensor memory, V is
-//                         read MN-major from its TMA tile;
+//                         through 4 shared-memory stages (2 at D = 128);
+//   warpgroup 2, warp 9   MMA issue of S_t = Q_t K^T (M=128, N=128, K=D);
+//   warps 10, 11          MMA issue of O_t += P_t V (M=128, N=64 per
+//                         64-column half of O, K=128) for t = A, B; S, P and
+//                         O live in tensor memory, V is read MN-major from its
+//                         TMA tile;
 //   warpgroup 0 / 1       softmax of tile A / B: a thread owns one query row
 //                         (one TMEM lane).  It loads the row's 128 scores into
 //                         registers and at once hands the S columns back, so
 //                         the tensor core computes the next S while the
-//                         exponentials of this one run.  P (bf16) goes back to
-//                         tensor memory in two halves of 64 keys, each of
-//                         which releases its half of the P.V product.
+//                         exponentials of this one run (at D = 128, where P
+//                         takes over the S columns, once P.V has read P).
+//                         P (bf16) goes back to tensor memory in two halves
+//                         of 64 keys, each of which releases its half of the
+//                         P.V product.
 // The running maximum is raised lazily: only when a tile's maximum exceeds it
 // by more than 2^8 is O rescaled (in TMEM).  KV tiles entirely above the
 // diagonal are never loaded; only tiles that cross it are masked.  Warpgroup
@@ -43,55 +46,79 @@ namespace {
 
 constexpr int BM = 128;                    // query rows per tile (TMEM lanes)
 constexpr int BN = 128;                    // keys per KV tile
-constexpr int HD = 64;                     // head dimension
-constexpr int TILE_BYTES = BM * HD * 2;    // one 128 x 64 bf16 tile: 16 KiB
 constexpr int NTHR = 384;                  // three warpgroups
-// Register split.  The kernel is compiled for 384 threads x 168 registers
-// (65,536 / 384, rounded down to a multiple of 8); the shares below must not
-// add up to more: 128 x 72 + 256 x 208 = 62,464 <= 64,512.  (The MMA-issue
-// code needs about 72 registers without spilling; a softmax thread holds a
-// 128-score row.)
-constexpr int REG_CTRL = 72, REG_SOFTMAX = 208;
-static_assert(128 * REG_CTRL + 256 * REG_SOFTMAX <= NTHR * 168, "register split exceeds the launch allocation");
-// tensor memory columns: S_A [0,128) S_B [128,256) O_A [256,320) O_B [320,384) P_A [384,448) P_B [448,512)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;
 constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
-constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
+constexpr uint32_t IDESC_O = idesc_bf16(BM, 64, false, true);  // one 64-column half of O per instruction
+constexpr int kMinShareTiles = 6;          // KV tiles per cluster share, at least
+constexpr int BOX_BYTES = 128 * 128;       // one TMA box: 128 rows x 64 bf16 columns (128 bytes), 16 KiB
 
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr int NST = 4;                          // K/V stages
-constexpr int kMinShareTiles = 6;               // KV tiles per cluster share, at least
-constexpr int OFF_Q = 0;                        // Q_A, Q_B
-constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // NST stages
-constexpr int OFF_V = OFF_K + NST * TILE_BYTES; // NST stages
-constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-// Split-KV exchange (after the main loop, over the K/V stages): a partial row
-// is (O[64], m, l) padded to 17 float4 chunks; a unit is 32 rows of one tile,
-// stored chunk-major ([chunk][row][4]) so that the 32 lanes of a warp write
-// one 512-byte run per remote store; the 8 units of a CTA are spread over the
-// cluster.
-constexpr int XCHUNKS = 17, XUNIT = XCHUNKS * 32 * 4;  // floats per unit
-// With ks CTAs in a cluster a rank finishes ceil(8/ks) units; the buffer
-// holds ks of those per rank, at most 14 units (ks = 7).
-static_assert(14 * XUNIT * 4 <= 2 * NST * TILE_BYTES, "exchange buffer fits in the K/V stages");
-// float offset of chunk c of row `lane` in unit (src, slot) of the exchange
-__device__ __forceinline__ int xidx(int src, int slot, int units_per_rank, int c, int lane) {
-  return (((src * units_per_rank + slot) * XCHUNKS + c) * 32 + lane) * 4;
+// Layout for head dimension HD (64 or 128).  A Q, K or V tile is HD/64 boxes
+// of 64 columns side by side in shared memory.
+//   tensor memory, HD = 64:  S_A [0,128) S_B [128,256) O_A [256,320) O_B [320,384)
+//                            P_A [384,448) P_B [448,512)
+//   tensor memory, HD = 128: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
+//                            P_t overwrites the first 64 columns of S_t (the
+//                            row's scores are in registers by then), so the
+//                            next S_t waits until P_t V has been computed
+//   shared memory: Q_A, Q_B, then NST stages of K and NST of V (4 stages at
+//                  HD = 64, 161 KB; 2 at HD = 128, 193 KB)
+template <int HD_>
+struct PfCfg {
+  static constexpr int HD = HD_;
+  static constexpr int NBOX = HD / 64;
+  static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
+  static constexpr int NST = HD == 64 ? 4 : 2;
+  static constexpr bool P_ALIAS = HD == 128;
+  static constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = P_ALIAS ? 0u : 384u;
+  static constexpr uint32_t P_STRIDE = P_ALIAS ? 128u : 64u;  // columns from P_A to P_B
+  // Register split.  The kernel is compiled for 384 threads x 168 registers
+  // (65,536 / 384, rounded down to a multiple of 8); the shares must not add
+  // up to more: 128 x 72 + 256 x 208 = 62,464 and 128 x 56 + 256 x 224 =
+  // 64,512 <= 64,512.  A softmax thread holds a 128-score row; at HD = 128 it
+  // also walks a 128-column O row (32 columns at a time), and with 208 it
+  // spilled, while the MMA-issue code fits in 56.
+  static constexpr int REG_CTRL = HD == 64 ? 72 : 56, REG_SOFTMAX = HD == 64 ? 208 : 224;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+  // mbarrier slots ([t] = per query tile)
+  //   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
+  //   B_P0[t]  P_t keys 0..63 stored            B_P1[t]  P_t keys 64..127 stored
+  //   B_O0[t]  P.V over keys 0..63 done         B_O1[t]  P.V over all keys done
+  //   B_DRAIN  after a timed-out wait: the MMA-issuing warps' work is done
+  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST,
+                       B_SC = B_S + 2, B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2,
+                       B_DRAIN = B_O1 + 2, N_BARS = B_DRAIN + 1;
+  static constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8;
+  // Split-KV exchange (after the main loop, over Q and the K/V stages): a
+  // partial row is (O[HD], m, l) padded to HD/4 + 1 float4 chunks; a unit is
+  // 32 rows of one tile, stored chunk-major ([chunk][row][4]) so that the 32
+  // lanes of a warp write one 512-byte run per remote store; the 8 units of a
+  // CTA are spread over the cluster.  With ks CTAs in a cluster a rank
+  // finishes ceil(8/ks) units and holds ks of those per rank.
+  static constexpr int XCHUNKS = HD / 4 + 1, XUNIT = XCHUNKS * 32 * 4;  // floats per unit
+  static constexpr int X_MAX_UNITS = OFF_BAR / (XUNIT * 4);
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+  static_assert(OFF_ABORT + 4 <= 256, "barrier area");
+  static_assert(HD == 64 || HD == 128, "head dimension");
+  static_assert(128 * REG_CTRL + 256 * REG_SOFTMAX <= NTHR * 168, "register split exceeds the launch allocation");
+};
+// Cluster sizes whose exchange fits: every size up to 8 at HD = 64 (at most
+// 14 units), 1-5 and 8 at HD = 128 (10 units for 5, 12 and 14 for 6 and 7).
+__host__ __device__ constexpr bool kv_split_fits(int units_max, int ks) {
+  return ks * ((8 + ks - 1) / ks) <= units_max;
 }
-
-// mbarrier slots ([t] = per query tile)
-//   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
-//   B_P0[t]  P_t keys 0..63 stored            B_P1[t]  P_t keys 64..127 stored
-//   B_O0[t]  P.V over keys 0..63 done         B_O1[t]  P.V over all keys done
-//   B_DRAIN  after a timed-out wait: the MMA-issuing warps' work is done
-constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST, B_SC = B_S + 2,
-              B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2, B_DRAIN = B_O1 + 2,
-              N_BARS = B_DRAIN + 1;
-constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8;
-static_assert(OFF_ABORT + 4 <= 256, "barrier area");
+static_assert(kv_split_fits(PfCfg<64>::X_MAX_UNITS, 7), "every cluster size fits at HD = 64");
+static_assert(kv_split_fits(PfCfg<128>::X_MAX_UNITS, 5) && kv_split_fits(PfCfg<128>::X_MAX_UNITS, 8),
+              "cluster sizes 5 and 8 fit at HD = 128");
+// float offset of chunk c of row `lane` in unit (src, slot) of the exchange
+template <int HD>
+__device__ __forceinline__ int xidx(int src, int slot, int units_per_rank, int c, int lane) {
+  return (((src * units_per_rank + slot) * PfCfg<HD>::XCHUNKS + c) * 32 + lane) * 4;
+}
 
 // Status of the prefill calls on this device (GQA_DEV_* bits), OR-accumulated
 // by every prefill kernel until gqa_attn_clear_prefill_status.
@@ -177,12 +204,19 @@ __device__ __forceinline__ void exp_half(const uint32_t* s, float2 c, float2 mm,
   }
 }
 
-// SPLIT: the pair's KV range is shared by a cluster of p.kv_splits CTAs
-// whose partial rows are merged through distributed shared memory.
-template <bool SPLIT>
+// HD: head dimension (64 or 128).  SPLIT: the pair's KV range is shared by a
+// cluster of p.kv_splits CTAs whose partial rows are merged through
+// distributed shared memory.
+template <int HD, bool SPLIT>
 __global__ void __launch_bounds__(NTHR, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using C = PfCfg<HD>;
+  constexpr int NBOX = C::NBOX, TILE_BYTES = C::TILE_BYTES, NST = C::NST;
+  constexpr int OFF_Q = C::OFF_Q, OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_BAR = C::OFF_BAR;
+  constexpr int B_Q = C::B_Q, B_KF = C::B_KF, B_VF = C::B_VF, B_KE = C::B_KE, B_S = C::B_S, B_SC = C::B_SC,
+                B_P0 = C::B_P0, B_P1 = C::B_P1, B_O0 = C::B_O0, B_O1 = C::B_O1, B_DRAIN = C::B_DRAIN;
+  constexpr uint32_t TM_S = C::TM_S, TM_O = C::TM_O, TM_P = C::TM_P;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -240,15 +274,15 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int nkv_max = j_hi - j_lo;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + OFF_TSLOT);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + OFF_ABORT);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + C::OFF_TSLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_ABORT);
 
   if (warp == 9) {
     tmem_alloc(tslot, TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 256) {
-    for (int i = 0; i < N_BARS; ++i) {
+    for (int i = 0; i < C::N_BARS; ++i) {
       const bool per_warp = (i >= B_SC && i < B_O0);  // arrivals of the 4 softmax warps of a tile
       const bool three = (i >= B_KE && i < B_KE + NST) || i == B_DRAIN;  // the three MMA-issuing warps
       mbar_init(&bars[i], per_warp ? 4 : three ? 3 : 1);
@@ -266,21 +300,31 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (p.q_lens == nullptr) grid_dependency_wait();
 
   if (warp >= 8) {
-    set_max_regs_dec<REG_CTRL>();
+    set_max_regs_dec<C::REG_CTRL>();
     if (warp == 8 && lane == 0) {
       // ---------------- TMA ----------------
       const int kv_head = b * p.Hkv + g;
       mbar_arrive_expect_tx(&bars[B_Q], 2 * TILE_BYTES);
-      tma_load_3d(smem + OFF_Q, &tmQ, 0, m0, b * p.Hq + h, &bars[B_Q]);
-      tma_load_3d(smem + OFF_Q + TILE_BYTES, &tmQ, 0, m0 + BM, b * p.Hq + h, &bars[B_Q]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx)
+          tma_load_3d(smem + OFF_Q + t * TILE_BYTES + bx * BOX_BYTES, &tmQ, bx * 64, m0 + t * BM, b * p.Hq + h,
+                      &bars[B_Q]);
       for (int j = 0; j < nkv_max; ++j) {
         const int st = j % NST;
         if (j >= NST) cta_wait(&bars[B_KE + st], uint32_t(j / NST - 1) & 1u, abort_flag, p.wait_limit_ns);
         if (*abort_flag) break;
         mbar_arrive_expect_tx(&bars[B_KF + st], TILE_BYTES);
-        tma_load_3d(smem + OFF_K + st * TILE_BYTES, &tmK, 0, (j_lo + j) * BN, kv_head, &bars[B_KF + st]);
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx)
+          tma_load_3d(smem + OFF_K + st * TILE_BYTES + bx * BOX_BYTES, &tmK, bx * 64, (j_lo + j) * BN, kv_head,
+                      &bars[B_KF + st]);
         mbar_arrive_expect_tx(&bars[B_VF + st], TILE_BYTES);
-        tma_load_3d(smem + OFF_V + st * TILE_BYTES, &tmV, 0, (j_lo + j) * BN, kv_head, &bars[B_VF + st]);
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx)
+          tma_load_3d(smem + OFF_V + st * TILE_BYTES + bx * BOX_BYTES, &tmV, bx * 64, (j_lo + j) * BN, kv_head,
+                      &bars[B_VF + st]);
       }
     } else if (warp == 9) {
       // ---------------- MMA issue: S_t = Q_t K^T ----------------
@@ -293,6 +337,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       const uint64_t kdesc = sdesc_sw128(smem_u32(smem + OFF_K));
       constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;  // descriptor units (16 B) per tile / stage
       constexpr uint64_t K_KSTEP = 32 >> 4;             // per 16-deep slice of the head dimension
+      constexpr uint64_t BOX_STEP = BOX_BYTES >> 4;     // per 64 dims (the next box)
       cta_wait(&bars[B_Q], 0, abort_flag, p.wait_limit_ns);
       for (int j = 0; j < nkv_max; ++j) {
         const int st = j % NST;
@@ -301,14 +346,21 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (j >= (t == 0 ? nkv0 : nkv1)) continue;
-          // S_t(j) overwrites S_t(j-1), which its softmax must have read
-          if (j > 0) cta_wait(&bars[B_SC + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
+          // S_t(j) overwrites S_t(j-1), which its softmax must have read,
+          // and, where P_t lives in the S_t columns, P_t(j-1), which the
+          // P.V product of tile j-1 must have read
+          if (j > 0) {
+            cta_wait(&bars[B_SC + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
+            if (C::P_ALIAS) cta_wait(&bars[B_O1 + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
+          }
           tc_fence_after();
           const uint64_t qd = qdesc + t * TILE_STEP;
           const uint32_t d = tmem + TM_S + t * 128;
-          mma_bf16_warp(d, qd, kd, IDESC_S, 0u);
 #pragma unroll
-          for (int kk = 1; kk < HD / 16; ++kk) mma_bf16_warp(d, qd + kk * K_KSTEP, kd + kk * K_KSTEP, IDESC_S, 1u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t koff = (kk / 4) * BOX_STEP + (kk % 4) * K_KSTEP;
+            mma_bf16_warp(d, qd + koff, kd + koff, IDESC_S, kk > 0 ? 1u : 0u);
+          }
           mma_commit_warp(&bars[B_S + t]);
         }
         mma_commit_warp(&bars[B_KE + st]);  // K of stage st is no longer needed once these are done
@@ -320,7 +372,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V));
       constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;
       constexpr uint64_t V_KSTEP = 2048 >> 4;  // 16 keys of the MN-major V tile
-      const uint32_t d = tmem + TM_O + t * 64, a = tmem + TM_P + t * 64;
+      constexpr uint64_t BOX_STEP = BOX_BYTES >> 4;  // the next 64 dims of V
+      const uint32_t d = tmem + TM_O + t * HD, a = tmem + TM_P + t * C::P_STRIDE;
       // Per-request lengths: the V map spans the whole cache, so the last KV
       // tile may hold rows past kv_len (anything, NaN included; their P is 0
       // but 0 * NaN is NaN).  Both P.V warps zero those rows first.
@@ -334,8 +387,12 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (j == j_zero) {
           unsigned char* vt = smem + OFF_V + st * TILE_BYTES;
           const int r0 = kv_len % BN;  // first row to clear (rows are 128 bytes; swizzle stays inside a row)
-          for (int i = (warp - 10) * 32 + lane; i < (BN - r0) * 8; i += 64)
-            *reinterpret_cast<uint4*>(vt + (r0 + i / 8) * 128 + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          const int per_box = (BN - r0) * 8;  // 16-byte chunks to clear in each box
+          for (int i = (warp - 10) * 32 + lane; i < per_box * NBOX; i += 64) {
+            const int bx = i / per_box, k = i % per_box;
+            *reinterpret_cast<uint4*>(vt + bx * BOX_BYTES + (r0 + k / 8) * 128 + (k % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
           fence_proxy_async_smem();
           asm volatile("bar.sync 1, 64;" ::: "memory");  // both P.V warps are done clearing
         }
@@ -347,8 +404,10 @@ __global__ void __launch_bounds__(NTHR, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ts_warp(d, a + half * 32 + kk * 8, vd + (half * 4 + kk) * V_KSTEP, IDESC_O,
-                               (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int bx = 0; bx < NBOX; ++bx)  // O columns [64 bx, 64 bx + 64) from V box bx
+                mma_bf16_ts_warp(d + bx * 64, a + half * 32 + kk * 8, vd + bx * BOX_STEP + (half * 4 + kk) * V_KSTEP,
+                                 IDESC_O, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
             mma_commit_warp(&bars[(half ? B_O1 : B_O0) + t]);
           }
         }
@@ -361,13 +420,13 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else {
     // ---------------- softmax of tile t = warp / 4 ----------------
-    set_max_regs_inc<REG_SOFTMAX>();
+    set_max_regs_inc<C::REG_SOFTMAX>();
     const int t = warp >> 2;
     const int nkv = t == 0 ? nkv0 : nkv1;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + TM_S + t * 128 + lane_off;
-    const uint32_t tO = tmem + TM_O + t * 64 + lane_off;
-    const uint32_t tP = tmem + TM_P + t * 64 + lane_off;
+    const uint32_t tO = tmem + TM_O + t * HD + lane_off;
+    const uint32_t tP = tmem + TM_P + t * C::P_STRIDE + lane_off;
     const int qi = m0 + t * BM + (tid & (BM - 1));
     const int last_key = p.causal ? min(off + qi, kv_len - 1) : kv_len - 1;
     const float c = p.qk_scale_log2;  // > 0 (the scale is checked on the host)
@@ -432,7 +491,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           const float alpha = resc ? fast_exp2(m_ref - tmax) : 1.f;
           if (resc) m_ref = tmax;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
+          for (int cc = 0; cc < HD / 32; ++cc) {
             uint32_t o[32];
             tmem_ld32(tO + cc * 32, o);
             tmem_wait_ld();
@@ -485,7 +544,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
         const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {  // 32 columns at a time keeps the register count down
+        for (int cc = 0; cc < HD / 32; ++cc) {  // 32 columns at a time keeps the register count down
           uint32_t o[32];
           tmem_ld32(tO + cc * 32, o);
           tmem_wait_ld();
@@ -509,14 +568,14 @@ __global__ void __launch_bounds__(NTHR, 1)
       // the CTA of the cluster that finishes this 32-row unit (unit u = warp,
       // finished by rank u % ks, slot u / ks), which merges the ks partials
       //   M = max m_s,  w_s = 2^(m_s - M),  O = sum w_s O_s / sum w_s l_s.
-      float* xbuf = reinterpret_cast<float*>(smem + OFF_K);  // the K/V stages are free after the loop
+      float* xbuf = reinterpret_cast<float*>(smem + OFF_Q);  // Q and the K/V stages are free after the loop
       cluster_sync_all();  // every CTA of the cluster is done with its stages
       {
         const int dst_rank = warp % ks, slot = warp / ks;
-        const float* loc = xbuf + xidx(rank, slot, upr, 0, lane);
+        const float* loc = xbuf + xidx<HD>(rank, slot, upr, 0, lane);
         const uint32_t ra = dsmem_addr(loc, uint32_t(dst_rank));
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           uint32_t o[32];
           if (nkv > 0) {
             tmem_ld32(tO + cc * 32, o);
@@ -531,30 +590,30 @@ __global__ void __launch_bounds__(NTHR, 1)
                       make_float4(__uint_as_float(o[4 * e4]), __uint_as_float(o[4 * e4 + 1]),
                                   __uint_as_float(o[4 * e4 + 2]), __uint_as_float(o[4 * e4 + 3])));
         }
-        dsmem_st4(ra + 16 * 512, make_float4(m_ref, lsum, 0.f, 0.f));
+        dsmem_st4(ra + (HD / 4) * 512, make_float4(m_ref, lsum, 0.f, 0.f));
       }
       cluster_sync_all();  // every partial has arrived
       if (warp % ks == rank && qi < q_len) {
         __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
         const int slot = warp / ks;
         float M = -INFINITY;
-        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[xidx(src, slot, upr, 16, lane)]);
+        for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[xidx<HD>(src, slot, upr, HD / 4, lane)]);
         float w_src[8], L = 0.f;
 #pragma unroll
         for (int src = 0; src < 8; ++src) {
-          const float ms = src < ks ? xbuf[xidx(src, slot, upr, 16, lane)] : -INFINITY;
+          const float ms = src < ks ? xbuf[xidx<HD>(src, slot, upr, HD / 4, lane)] : -INFINITY;
           w_src[src] = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
-          if (src < ks) L += xbuf[xidx(src, slot, upr, 16, lane) + 1] * w_src[src];
+          if (src < ks) L += xbuf[xidx<HD>(src, slot, upr, HD / 4, lane) + 1] * w_src[src];
         }
         const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / L;
 #pragma unroll
-        for (int e8 = 0; e8 < 8; ++e8) {  // 8 output columns at a time
+        for (int e8 = 0; e8 < HD / 8; ++e8) {  // 8 output columns at a time
           float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int src = 0; src < 8; ++src) {
             if (src < ks) {
-              const float4 v0 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, upr, 2 * e8, lane));
-              const float4 v1 = *reinterpret_cast<const float4*>(xbuf + xidx(src, slot, upr, 2 * e8 + 1, lane));
+              const float4 v0 = *reinterpret_cast<const float4*>(xbuf + xidx<HD>(src, slot, upr, 2 * e8, lane));
+              const float4 v1 = *reinterpret_cast<const float4*>(xbuf + xidx<HD>(src, slot, upr, 2 * e8 + 1, lane));
               const float w = w_src[src];
               acc8[0] += v0.x * w; acc8[1] += v0.y * w; acc8[2] += v0.z * w; acc8[3] += v0.w * w;
               acc8[4] += v1.x * w; acc8[5] += v1.y * w; acc8[6] += v1.z * w; acc8[7] += v1.w * w;
@@ -589,26 +648,26 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (warp == 9) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// Q, K, V as [heads][row_pitch rows][64] bf16 with only the first `rows` rows
+// Q, K, V as [heads][row_pitch rows][hd] bf16 with only the first `rows` rows
 // of a head readable (cache rows past kv_len arrive as zeros and add exactly
-// nothing to P.V); 128-row x 64-column boxes.
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_pitch, uint64_t heads) {
-  return encode_bf16_rows(map, base, HD, rows, row_pitch, heads, HD, 128);
+// nothing to P.V); boxes of 128 rows x 64 columns (128 bytes, the widest a
+// 128-byte swizzle takes), hd / 64 of them side by side for a tile.
+bool make_map(CUtensorMap* map, const void* base, int hd, uint64_t rows, uint64_t row_pitch, uint64_t heads) {
+  return encode_bf16_rows(map, base, uint64_t(hd), rows, row_pitch, heads, 64, 128);
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  if (a.D != HD) return cudaErrorNotSupported;
+template <int HD>
+cudaError_t launch_prefill_hd(const PrefillArgs& a, cudaStream_t stream) {
+  using C = PfCfg<HD>;
   CUtensorMap tq, tk, tv;
   // uniform lengths: the K/V maps end at kv_len, so rows past it arrive as
   // zeros; per-request lengths: the maps span the whole buffers and the
   // kernel masks and clears what lies past each request's lengths
   const bool varlen = a.q_lens != nullptr;
   const uint64_t q_rows = a.q_len, kv_rows = varlen ? uint64_t(a.S_cap) : uint64_t(a.kv_len);
-  if (!make_map(&tq, a.q, q_rows, a.q_len, uint64_t(a.B) * a.Hq) ||
-      !make_map(&tk, a.k, kv_rows, a.S_cap, uint64_t(a.B) * a.Hkv) ||
-      !make_map(&tv, a.v, kv_rows, a.S_cap, uint64_t(a.B) * a.Hkv))
+  if (!make_map(&tq, a.q, HD, q_rows, a.q_len, uint64_t(a.B) * a.Hq) ||
+      !make_map(&tk, a.k, HD, kv_rows, a.S_cap, uint64_t(a.B) * a.Hkv) ||
+      !make_map(&tv, a.v, HD, kv_rows, a.S_cap, uint64_t(a.B) * a.Hkv))
     return cudaErrorInvalidValue;
   PrefillParams p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -629,23 +688,27 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   // wave and every share at kMinShareTiles KV tiles or more.  (Beyond one
   // wave a cluster has to wait for SMs of one GPC to free up together, which
   // costs more than the split gains: T=4097 took 49 us unsplit, 68 us split
-  // in two.)
+  // in two.)  At HD = 128 the exchange holds no more than 5 CTAs' units
+  // except for 8, so 6 and 7 become 5.
   {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long pairs = long(a.B) * a.Hq * p.n_pairs;
     const int kv_tiles = (a.kv_len + BN - 1) / BN;
-    long ks = 1;
-    if (pairs * 2 <= sms) ks = std::min<long>({8L, sms / pairs, std::max<long>(1L, kv_tiles / kMinShareTiles)});
+    int ks = 1;
+    if (pairs * 2 <= sms)
+      ks = int(std::min<long>({8L, sms / pairs, std::max<long>(1L, kv_tiles / kMinShareTiles)}));
     if (const int v = prefill_kv_split_override(); v >= 1 && v <= 8) ks = v;  // tuning and tests only
-    p.kv_splits = int(ks);
+    while (!kv_split_fits(C::X_MAX_UNITS, ks)) --ks;
+    p.kv_splits = ks;
   }
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(prefill_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -653,7 +716,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHR);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -665,10 +728,18 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   cfg.attrs = attr;
   if (p.kv_splits == 1) {
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<false>, tq, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, false>, tq, tk, tv, p);
   }
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, true>, tq, tk, tv, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.D == 64) return launch_prefill_hd<64>(a, stream);
+  if (a.D == 128) return launch_prefill_hd<128>(a, stream);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace gqa

@@ -198,7 +198,7 @@ GQA_ATTN_API int gqa_attn_decode_paged(const void* q, const void* k_new, const v
  *   kv_lens   q_lens[b] into [0, min(Tq_cap, kv_lens[b])]
  *   causal    1: query i of request b sees keys j <= i + kv_lens[b] - q_lens[b];
  *             0: all kv_lens[b] keys
- * D = 64 (bf16).  Other errors as for gqa_attn_prefill.
+ * D = 64 or 128 (bf16).  Other errors as for gqa_attn_prefill.
  * ------------------------------------------------------------------------- */
 GQA_ATTN_API int gqa_attn_prefill_varlen(const void* q, const void* k, const void* v, void* o,
                                          const int32_t* q_lens, const int32_t* kv_lens, int B, int Hq,
@@ -366,7 +366,7 @@ GQA_ATTN_API int gqa_attn_decode_q4(const void* q, const uint8_t* k_codes,
  *            the same for every request
  *   causal   1: key j visible to query row i iff j <= i + kv_len - q_len;
  *            0: every key j < kv_len visible
- *   dtype    GQA_BF16 (fp32 accumulation).   D == 64.
+ *   dtype    GQA_BF16 (fp32 accumulation).   D == 64 or 128.
  *   limits   q_len <= 65535 * 256, B * Hq < 2^31 (else GQA_ERR_INVALID_ARG).
  * Errors: as for decode; a dtype / D without a kernel is GQA_ERR_UNSUPPORTED.
  * Nothing is allocated; the call is asynchronous on `stream`.
