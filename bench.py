@@ -840,23 +840,30 @@ def _case_inputs(name, device):
         return (lambda st: binding_mod().gqa_attn_decode_layers(q, k, v, o, None, D ** -0.5, ws, max_kv_len=S_HEAD,
                                                                 stream=st)), nbytes, "bytes"
     if name.startswith("prefill-"):
-        parts = name.split("-")[1:]           # prefill-T4097 or prefill-q512-kv4096
+        # prefill-T4097, prefill-q512-kv4096 (Qwen2.5-0.5B heads, D=64) or
+        # prefill-d128-T4097 (Qwen2.5-7B heads, D=128)
+        parts = name.split("-")[1:]
+        Hq, Hkv, D = 14, 2, 64
+        if parts[0] == "d128":
+            Hq, Hkv, D = 28, 4, 128
+            parts = parts[1:]
         if len(parts) == 1:
             q_len = kv_len = int(parts[0][1:])
         else:
             q_len, kv_len = int(parts[0][1:]), int(parts[1][2:])
-        q = inputs.randn((1, 14, q_len, 64), inputs.tensor_seed(0, 0), torch.bfloat16, device)
-        k = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 1), torch.bfloat16, device)
-        v = inputs.randn((1, 2, kv_len, 64), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+        q = inputs.randn((1, Hq, q_len, D), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+        k = inputs.randn((1, Hkv, kv_len, D), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+        v = inputs.randn((1, Hkv, kv_len, D), inputs.tensor_seed(0, 2), torch.bfloat16, device)
         o = torch.empty_like(q)
-        flops = metrics.prefill_flops(14, 64, q_len, kv_len, causal=True)
-        return (lambda st: binding_mod().gqa_attn_prefill(q, k, v, o, kv_len, 0.125, True, st)), flops, "flop"
+        flops = metrics.prefill_flops(Hq, D, q_len, kv_len, causal=True)
+        return (lambda st: binding_mod().gqa_attn_prefill(q, k, v, o, kv_len, D ** -0.5, True, st)), flops, "flop"
     raise SystemExit(f"unknown kernel case {name!r}")
 
 
 KERNEL_CASES = ("decode-f32-S32768", "decode-bf16-S32768", "decode-bf16-ragged-B64", "decode-bf16-paged-B64",
                 "q4-B4-S16384", "quantize-B4-S16384",
                 "prefill-T4097", "prefill-T16384", "prefill-q512-kv4096", "varlen-prefill-B16",
+                "prefill-d128-T4097", "prefill-d128-T16384",
                 "decode-f32-layers8-S32768")
 
 
@@ -1102,6 +1109,17 @@ def main():
         if cpu is not None:
             pf[3]["cpu_oracle"] = cpu["prefill_T16384"]
         line["prefill_causal_qwen05b_bf16"] = pf
+        # head dimension 128 at the Qwen2.5-7B head geometry (28 layers per step)
+        pf128 = [prefill_point(binding, T, T, device, stream, flush, bf16_peak, NL=28, Hq=28, Hkv=4, D=128)
+                 for T in (4097, 16384)]
+        pf128.append(prefill_point(binding, 512, 4096, device, stream, flush, bf16_peak, NL=28, Hq=28, Hkv=4,
+                                   D=128))
+        line["prefill_causal_qwen7b_d128_bf16"] = pf128
+        line["roofline_prefill_d128"] = {"bound": "tensor", "achieved": pf128[1]["TFLOPs"], "peak": bf16_peak,
+                                         "unit": "TFLOP/s", "frac": pf128[1]["frac_of_bf16_peak"],
+                                         "traffic": recorded_traffic("prefill.cu", "prefill_causal_d128_T16384"),
+                                         "kernel": "prefill_kernel<128> (T=16384 causal, 28 layer launches per step)",
+                                         "peak_source": peak_src + " bf16 burst"}
         big = pf[3]
         line["roofline_prefill"] = {"bound": "tensor", "achieved": big["TFLOPs"], "peak": bf16_peak,
                                     "unit": "TFLOP/s", "frac": big["frac_of_bf16_peak"],

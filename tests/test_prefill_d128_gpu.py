@@ -93,6 +93,24 @@ def test_causal_prefill_4097_7b_one_head_per_kv_head():
     check_full(q, k, v, T, True, heads=(0, 9, 18, 27))
 
 
+def test_causal_prefill_16384_7b_two_heads_every_row():
+    """Every row of query heads 0 and 27 (KV heads 0 and 3).  Rows [r0, r1)
+    of a causal prefill are a chunk of r1 - r0 queries aligned to the end of
+    keys [0, r1), so the oracle runs in chunks of 2048 rows."""
+    T = 16384
+    q, k, v = case(1, 28, 4, T, T, layer=3)
+    o = binding.prefill(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    on = f64(o)
+    for h in (0, 27):
+        g = h // 7
+        qh, kh, vh = f64(q[:, h:h + 1]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1])
+        for r0 in range(0, T, 2048):
+            r1 = r0 + 2048
+            ref = oracle.attention(qh[:, :, r0:r1], kh[:, :, :r1], vh[:, :, :r1], scale=SCALE, causal=True)["o"]
+            parity.check(on[:, h:h + 1, r0:r1], ref, "bf16", f"head {h} rows {r0}..{r1}")
+
+
 def test_chunked_prefill_512_at_3584_7b():
     q, k, v = case(1, 28, 4, 512, 4096, layer=5)
     check_full(q, k, v, 4096, True)
