@@ -55,6 +55,7 @@ EXPORTED = (
     "gqa_attn_decode_num_splits",
     "gqa_attn_version",
     "gqa_attn_set_plan_override",
+    "gqa_attn_set_prefill_interleave_override",
     "gqa_attn_read_prefill_status",
     "gqa_attn_clear_prefill_status",
 )
@@ -123,6 +124,8 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_version.restype = i32
     L.gqa_attn_set_plan_override.argtypes = [i32, i32]
     L.gqa_attn_set_plan_override.restype = i32
+    L.gqa_attn_set_prefill_interleave_override.argtypes = [i32]
+    L.gqa_attn_set_prefill_interleave_override.restype = i32
     L.gqa_attn_read_prefill_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
     L.gqa_attn_read_prefill_status.restype = i32
     L.gqa_attn_clear_prefill_status.argtypes = [vp]
@@ -177,14 +180,24 @@ def gqa_attn_set_plan_override(decode_splits=0, prefill_kv_split=0) -> None:
            "gqa_attn_set_plan_override")
 
 
+def gqa_attn_set_prefill_interleave_override(from_pair=-1) -> None:
+    """Tuning and tests only: prefill pairs from index from_pair on run as
+    single query tiles whose keys the two softmax warpgroups take in turn
+    (0 = every tile; past the last pair = none; negative = the planner)."""
+    _check(lib().gqa_attn_set_prefill_interleave_override(int(from_pair)),
+           "gqa_attn_set_prefill_interleave_override")
+
+
 @contextlib.contextmanager
-def plan_override(decode_splits=0, prefill_kv_split=0):
-    """``with plan_override(...)``: the override for the block, then none."""
+def plan_override(decode_splits=0, prefill_kv_split=0, prefill_interleave_from=-1):
+    """``with plan_override(...)``: the overrides for the block, then none."""
     gqa_attn_set_plan_override(decode_splits, prefill_kv_split)
+    gqa_attn_set_prefill_interleave_override(prefill_interleave_from)
     try:
         yield
     finally:
         gqa_attn_set_plan_override(0, 0)
+        gqa_attn_set_prefill_interleave_override(-1)
 
 
 def gqa_attn_decode(q, k, v, o, kv_lens, scale, workspace, max_kv_len=None, stream=None):

@@ -31,6 +31,8 @@ static std::atomic<int> g_decode_splits_override{0};
 static std::atomic<int> g_prefill_kv_split_override{0};
 
 int prefill_kv_split_override() { return g_prefill_kv_split_override.load(std::memory_order_relaxed); }
+static std::atomic<int> g_prefill_interleave_override{-1};
+int prefill_interleave_override() { return g_prefill_interleave_override.load(std::memory_order_relaxed); }
 
 // Chooses how many key splits each (request, KV head) gets so that the grid
 // covers at most ctas_per_sm CTAs per SM (one wave) when requests are few and
@@ -149,6 +151,11 @@ GQA_ATTN_API int gqa_attn_set_plan_override(int decode_splits, int prefill_kv_sp
   if (decode_splits < 0 || prefill_kv_split < 0 || prefill_kv_split > 8) return GQA_ERR_INVALID_ARG;
   g_decode_splits_override.store(decode_splits, std::memory_order_relaxed);
   g_prefill_kv_split_override.store(prefill_kv_split, std::memory_order_relaxed);
+  return GQA_OK;
+}
+
+GQA_ATTN_API int gqa_attn_set_prefill_interleave_override(int from_pair) {
+  g_prefill_interleave_override.store(from_pair < 0 ? -1 : from_pair, std::memory_order_relaxed);
   return GQA_OK;
 }
 

@@ -48,6 +48,8 @@ int device_sm_count();
 // The prefill KV-split cluster size forced by gqa_attn_set_plan_override, or
 // 0 (the planner decides).
 int prefill_kv_split_override();
+// Forced first interleaved pair of prefill (>= 0), or -1 for the planner's choice.
+int prefill_interleave_override();
 
 // Shape, dtype and pointer checks shared by gqa_attn_decode and
 // gqa_attn_decode_noalloc (everything but the workspace); GQA_OK or an error.

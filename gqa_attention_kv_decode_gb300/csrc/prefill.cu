@@ -32,9 +32,14 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdlib>
+#include <functional>
+#include <map>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "gqa_attn.h"
 #include "internal.h"
@@ -83,7 +88,9 @@ struct PfCfg {
   static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+  static constexpr int OFF_ILV = OFF_BAR + 256;              // (m, l) of 128 rows, single-tile units
+  static constexpr int OFF_LIM = OFF_ILV + 1024;             // per softmax thread: last key - first key
+  static constexpr int SMEM_BYTES = OFF_LIM + 1024 + 1024;   // + alignment slack
   // mbarrier slots ([t] = per query tile)
   //   B_S[t]   S_t ready (MMA commit)           B_SC[t]  S_t read by all 4 warps
   //   B_P0[t]  P_t keys 0..63 stored            B_P1[t]  P_t keys 64..127 stored
@@ -92,7 +99,7 @@ struct PfCfg {
   static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST,
                        B_SC = B_S + 2, B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2,
                        B_DRAIN = B_O1 + 2, N_BARS = B_DRAIN + 1;
-  static constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8;
+  static constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8, OFF_UNIT = OFF_ABORT + 4;
   // Split-KV exchange (after the main loop, over Q and the K/V stages): a
   // partial row is (O[HD], m, l) padded to HD/4 + 1 float4 chunks; a unit is
   // 32 rows of one tile, stored chunk-major ([chunk][row][4]) so that the 32
@@ -102,7 +109,7 @@ struct PfCfg {
   static constexpr int XCHUNKS = HD / 4 + 1, XUNIT = XCHUNKS * 32 * 4;  // floats per unit
   static constexpr int X_MAX_UNITS = OFF_BAR / (XUNIT * 4);
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-  static_assert(OFF_ABORT + 4 <= 256, "barrier area");
+  static_assert(OFF_UNIT + 8 <= 256, "barrier area");
   static_assert(HD == 64 || HD == 128, "head dimension");
   static_assert(128 * REG_CTRL + 256 * REG_SOFTMAX <= NTHR * 168, "register split exceeds the launch allocation");
 };
@@ -127,6 +134,11 @@ __device__ uint32_t g_prefill_status = 0;
 struct PrefillParams {
   __nv_bfloat16* o;
   int Hq, Hkv, n_rep, q_len, kv_len, n_pairs, causal;
+  // Work units on grid y (see prefill_kernel): pairs of query tiles below
+  // ilv_from, and single query tiles of the pairs from ilv_from on, whose KV
+  // tiles the two softmax warpgroups share out (even / odd); n_first pairs
+  // are scheduled before those single tiles.
+  int n_tiles, ilv_from, n_first;
   int kv_splits;        // CTAs of a cluster sharing one pair's KV tiles (1 to 8)
   float qk_scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
@@ -183,6 +195,8 @@ __device__ __forceinline__ void set_max_regs_dec() {
 // Named barriers 2 and 3 alternate the exponentials of the two softmax
 // warpgroups (256 threads each: 128 wait, the other 128 arrive).
 constexpr int BAR_TURN_A = 2, BAR_TURN_B = 3;
+// Named barrier 4: slot 1 of a single-tile unit has left its (m, l) for slot 0.
+constexpr int BAR_ILV = 4;
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -206,8 +220,10 @@ __device__ __forceinline__ void exp_half(const uint32_t* s, float2 c, float2 mm,
 
 // HD: head dimension (64 or 128).  SPLIT: the pair's KV range is shared by a
 // cluster of p.kv_splits CTAs whose partial rows are merged through
-// distributed shared memory.
-template <int HD, bool SPLIT>
+// distributed shared memory.  ILV: the grid also holds single-tile units (see
+// below); a launch without them uses the ILV = false kernel, whose code is
+// that of pairs alone (the unit bookkeeping costs the pair loop registers).
+template <int HD, bool SPLIT, bool ILV>
 __global__ void __launch_bounds__(NTHR, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -223,18 +239,33 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // Blocks start in the order of their linear index (x fastest): with the
-  // pair rank on y, the longest causal pairs of every head are scheduled
-  // first and the short ones fill in behind them.
+  // Blocks start in the order of their linear index (x fastest), and the
+  // units on y are ordered longest first for a causal mask, so the short
+  // ones fill in behind the long ones.  A unit is either a pair of query
+  // tiles (A, B) over the same KV tiles, or a single query tile ("ilv")
+  // whose KV tiles are dealt to the two softmax warpgroups in turn (slot 0
+  // the even ones, slot 1 the odd ones), which halves the iterations of the
+  // longest causal tiles; the two slots' partial rows are combined at the
+  // end.  Order on y: n_first pairs (ilv_from - 1 downwards), the single
+  // tiles (the last tile downwards), then the remaining pairs.
   const int ks = SPLIT ? p.kv_splits : 1;
   const int upr = (8 + ks - 1) / ks;  // exchange units a rank finishes
   const int rank = SPLIT ? int(cluster_rank()) : 0;
-  const int pair = p.n_pairs - 1 - int(blockIdx.y);
+  static_assert(!(SPLIT && ILV), "a cluster split runs pairs only");
+  bool ilv = false;
+  int m0;
+  if constexpr (ILV) {
+    const int n_ilv = max(0, p.n_tiles - 2 * p.ilv_from);
+    const int y = int(blockIdx.y);
+    ilv = y >= p.n_first && y < p.n_first + n_ilv;
+    m0 = ilv ? (p.n_tiles - 1 - (y - p.n_first)) * BM : (p.ilv_from - 1 - (y < p.n_first ? y : y - n_ilv)) * 2 * BM;
+  } else {
+    m0 = (p.n_pairs - 1 - int(blockIdx.y)) * 2 * BM;
+  }
   const int bh = int(blockIdx.x) / ks;  // a cluster = ks consecutive x
   const int h = bh % p.Hq;
   const int b = bh / p.Hq;
   const int g = h / p.n_rep;
-  const int m0 = pair * 2 * BM;
   // Launched with programmatic stream serialisation: the next grid in the
   // stream may start launching at once (its CTAs wait in the same way), and
   // nothing the previous grid writes is read or written before it is done.
@@ -265,17 +296,23 @@ __global__ void __launch_bounds__(NTHR, 1)
   // The pair's KV tiles [0, nkv_all) are cut into ks contiguous shares; this
   // CTA takes share `rank`, [j_lo, j_hi).  Below, j counts tiles of the share
   // (barrier phases, stages) and j_lo + j is the tile's position in the keys.
-  const int nkv_a = nkv_for(m0), nkv_b = nkv_for(m0 + BM);
+  // nkv0, nkv1: the KV tiles of slot 0 and slot 1 (tiles A and B of a pair;
+  // the even and odd tiles of a single-tile unit).
+  const int nkv_a = nkv_for(m0), nkv_b = ilv ? 0 : nkv_for(m0 + BM);
   const int nkv_all = max(nkv_a, nkv_b);
   const int j_lo = SPLIT ? nkv_all * rank / ks : 0;
   const int j_hi = SPLIT ? nkv_all * (rank + 1) / ks : nkv_all;
-  const int nkv0 = SPLIT ? max(0, min(nkv_a, j_hi) - j_lo) : nkv_a;
-  const int nkv1 = SPLIT ? max(0, min(nkv_b, j_hi) - j_lo) : nkv_b;
+  const int nkv0 = SPLIT ? max(0, min(nkv_a, j_hi) - j_lo) : ilv ? (nkv_all + 1) / 2 : nkv_a;
+  const int nkv1 = SPLIT ? max(0, min(nkv_b, j_hi) - j_lo) : ilv ? nkv_all / 2 : nkv_b;
   const int nkv_max = j_hi - j_lo;
+  // KV tile j of the unit belongs to slot t as the slot's iteration li
+  auto active = [&](int j, int t) -> bool { return ilv ? (j & 1) == t : j < (t == 0 ? nkv0 : nkv1); };
+  auto local_it = [&](int j) -> int { return ilv ? j >> 1 : j; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + C::OFF_TSLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_ABORT);
+  volatile int* unit_info = reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_UNIT);
 
   if (warp == 9) {
     tmem_alloc(tslot, TMEM_COLS);
@@ -288,6 +325,10 @@ __global__ void __launch_bounds__(NTHR, 1)
       mbar_init(&bars[i], per_warp ? 4 : three ? 3 : 1);
     }
     *abort_flag = 0;
+    if (ILV) {
+      unit_info[0] = m0;  // read back by the softmax epilogue (see there)
+      unit_info[1] = int(ilv);
+    }
     fence_barrier_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
@@ -304,9 +345,9 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (warp == 8 && lane == 0) {
       // ---------------- TMA ----------------
       const int kv_head = b * p.Hkv + g;
-      mbar_arrive_expect_tx(&bars[B_Q], 2 * TILE_BYTES);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
+      const int n_q = ilv ? 1 : 2;  // a single-tile unit reads Q_A only
+      mbar_arrive_expect_tx(&bars[B_Q], n_q * TILE_BYTES);
+      for (int t = 0; t < n_q; ++t)
 #pragma unroll
         for (int bx = 0; bx < NBOX; ++bx)
           tma_load_3d(smem + OFF_Q + t * TILE_BYTES + bx * BOX_BYTES, &tmQ, bx * 64, m0 + t * BM, b * p.Hq + h,
@@ -345,16 +386,17 @@ __global__ void __launch_bounds__(NTHR, 1)
         const uint64_t kd = kdesc + st * TILE_STEP;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j >= (t == 0 ? nkv0 : nkv1)) continue;
-          // S_t(j) overwrites S_t(j-1), which its softmax must have read,
-          // and, where P_t lives in the S_t columns, P_t(j-1), which the
-          // P.V product of tile j-1 must have read
-          if (j > 0) {
-            cta_wait(&bars[B_SC + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
-            if (C::P_ALIAS) cta_wait(&bars[B_O1 + t], uint32_t(j - 1) & 1u, abort_flag, p.wait_limit_ns);
+          if (!active(j, t)) continue;
+          const int li = local_it(j);
+          // S_t(li) overwrites S_t(li-1), which its softmax must have read,
+          // and, where P_t lives in the S_t columns, P_t(li-1), which the
+          // P.V product of iteration li-1 must have read
+          if (li > 0) {
+            cta_wait(&bars[B_SC + t], uint32_t(li - 1) & 1u, abort_flag, p.wait_limit_ns);
+            if (C::P_ALIAS) cta_wait(&bars[B_O1 + t], uint32_t(li - 1) & 1u, abort_flag, p.wait_limit_ns);
           }
           tc_fence_after();
-          const uint64_t qd = qdesc + t * TILE_STEP;
+          const uint64_t qd = qdesc + (ilv ? 0 : t) * TILE_STEP;
           const uint32_t d = tmem + TM_S + t * 128;
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
@@ -368,7 +410,6 @@ __global__ void __launch_bounds__(NTHR, 1)
     } else if (warp >= 10) {
       // ---------------- MMA issue: O_t += P_t V, t = warp - 10 ----------------
       const int t = warp - 10;
-      const int nkv = t == 0 ? nkv0 : nkv1;
       const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V));
       constexpr uint64_t TILE_STEP = TILE_BYTES >> 4;
       constexpr uint64_t V_KSTEP = 2048 >> 4;  // 16 keys of the MN-major V tile
@@ -396,18 +437,19 @@ __global__ void __launch_bounds__(NTHR, 1)
           fence_proxy_async_smem();
           asm volatile("bar.sync 1, 64;" ::: "memory");  // both P.V warps are done clearing
         }
-        if (j < nkv) {
+        if (active(j, t)) {
+          const int li = local_it(j);
           const uint64_t vd = vdesc + st * TILE_STEP;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            cta_wait(&bars[(half ? B_P1 : B_P0) + t], uint32_t(j) & 1u, abort_flag, p.wait_limit_ns);
+            cta_wait(&bars[(half ? B_P1 : B_P0) + t], uint32_t(li) & 1u, abort_flag, p.wait_limit_ns);
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
               for (int bx = 0; bx < NBOX; ++bx)  // O columns [64 bx, 64 bx + 64) from V box bx
                 mma_bf16_ts_warp(d + bx * 64, a + half * 32 + kk * 8, vd + bx * BOX_STEP + (half * 4 + kk) * V_KSTEP,
-                                 IDESC_O, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                                 IDESC_O, (li > 0 || half > 0 || kk > 0) ? 1u : 0u);
             mma_commit_warp(&bars[(half ? B_O1 : B_O0) + t]);
           }
         }
@@ -427,9 +469,24 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t tS = tmem + TM_S + t * 128 + lane_off;
     const uint32_t tO = tmem + TM_O + t * HD + lane_off;
     const uint32_t tP = tmem + TM_P + t * C::P_STRIDE + lane_off;
-    const int qi = m0 + t * BM + (tid & (BM - 1));
-    const int last_key = p.causal ? min(off + qi, kv_len - 1) : kv_len - 1;
     const float c = p.qk_scale_log2;  // > 0 (the scale is checked on the host)
+    // Masking.  Key n0_first + j * n0_step is the first of this slot's j-th
+    // KV tile; the row's last visible key is last_key.  Kept through the
+    // loop is only j_diag, the first iteration whose tile the diagonal (or
+    // kv_len) may cross for this row; last_key - n0_first waits in shared
+    // memory for the few iterations that mask (the loop holds a whole score
+    // row in registers and has none to spare).
+    // (ILV kernel; pairs alone keep qi and last_key and mask tile j iff
+    // (j_lo + j) * BN + BN - 1 > last_key)
+    const int qi = m0 + (ilv ? 0 : t * BM) + (tid & (BM - 1));
+    const int last_key = p.causal ? min(off + qi, kv_len - 1) : kv_len - 1;
+    int j_diag = 0;
+    if constexpr (ILV) {
+      const int n0_first = (ilv ? t : 0) * BN, n0_step = ilv ? 2 * BN : BN;
+      const int x = last_key - (BN - 1) - n0_first;  // tile j is masked iff j * n0_step > x
+      j_diag = x < 0 ? 0 : x / n0_step + 1;
+      reinterpret_cast<int*>(smem + C::OFF_LIM)[tid] = last_key - n0_first;
+    }
     float m_ref = -INFINITY, lsum = 0.f;
     // The two warpgroups share the schedulers, the XU and the FMA pipe; run
     // together their exponentials take twice as long while their P stores
@@ -456,12 +513,15 @@ __global__ void __launch_bounds__(NTHR, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SC + t]);  // the S columns may be overwritten now
 
-      const int n0 = (j_lo + j) * BN;
-      if (__any_sync(0xffffffffu, n0 + BN - 1 > last_key)) {  // the diagonal (or the end) crosses this tile
-        // mask, then take the maximum again over what is left
+      const bool cross = ILV ? j >= j_diag : (j_lo + j) * BN + BN - 1 > last_key;
+      if (__any_sync(0xffffffffu, cross)) {  // the diagonal (or the end) crosses this tile
+        // mask (keys past last_key), then take the maximum again over what is left
+        const int lim = ILV ? reinterpret_cast<const volatile int*>(smem + C::OFF_LIM)[tid] -
+                                  j * (unit_info[1] ? 2 * BN : BN)
+                            : last_key - (j_lo + j) * BN;  // last_key - (first key of the tile)
 #pragma unroll
         for (int e = 0; e < BN; ++e)
-          if (n0 + e > last_key) s[e] = 0xff800000u;  // -inf
+          if (e > lim) s[e] = 0xff800000u;  // -inf
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int e = 0; e < BN; e += 8) {
@@ -476,9 +536,10 @@ __global__ void __launch_bounds__(NTHR, 1)
       const float tmax = max3f(rmx[0], rmx[1], fmaxf(rmx[2], rmx[3])) * c;
       if (j == 0) {
         // The first tile of the share.  Without a split it holds key 0, which
-        // every row sees; with one, a row may see no key of the share at all
-        // (then every later tile of the share is masked for it too): its
-        // reference stays -inf and its exponentials use 0 instead.
+        // every row sees; with one (or for the odd KV tiles of a single-tile
+        // unit), a row may see no key of the share at all (then every later
+        // tile of the share is masked for it too): its reference stays -inf
+        // and its exponentials use 0 instead.
         m_ref = tmax;
       } else {
         const bool resc = tmax > m_ref + 8.f;
@@ -503,7 +564,9 @@ __global__ void __launch_bounds__(NTHR, 1)
           lsum *= alpha;
         }
       }
-      const float m_use = (SPLIT && m_ref == -INFINITY) ? 0.f : m_ref;
+      // (-inf only for a row that has seen no key of this slot yet, possible
+      // with a KV split or for the odd tiles of a single-tile unit)
+      const float m_use = ((SPLIT || ILV) && m_ref == -INFINITY) ? 0.f : m_ref;
       float mu = m_use;
       if (j < nmin) named_bar_sync(t == 0 ? BAR_TURN_A : BAR_TURN_B, 256);  // this warpgroup's turn
       // the exponentials depend on mu: keep the compiler from starting them
@@ -539,16 +602,69 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
 
     // ---- epilogue: O / l, bf16, to global memory ----
-    if (!SPLIT) {
+    // The unit's first query row and kind, read back from shared memory
+    // rather than kept in registers through the loop, which uses nearly all
+    // of this warpgroup's registers.
+    const bool ilv_e = ILV && unit_info[1] != 0;
+    const int qi_e = ILV ? unit_info[0] + (ilv_e ? 0 : t * BM) + (tid & (BM - 1)) : qi;
+    if (ILV && ilv_e) {
+      // Single-tile unit: slot 1 hands its rows' (m, l) to slot 0 through
+      // shared memory; slot 0 reads both O accumulators from tensor memory
+      // (its warps reach the same lanes) and combines them:
+      //   M = max(m0, m1),  w_s = 2^(m_s - M),  O = (w0 O0 + w1 O1) / (w0 l0 + w1 l1).
+      float2* mlx = reinterpret_cast<float2*>(smem + C::OFF_ILV);
+      if (t == 1) {
+        mlx[tid & (BM - 1)] = make_float2(m_ref, lsum);
+        tc_fence_before();
+        named_bar_arrive(BAR_ILV, 256);
+      } else {
+        named_bar_sync(BAR_ILV, 256);
+        tc_fence_after();
+        const float2 x1 = mlx[tid & (BM - 1)];
+        const bool has1 = nkv1 > 0;  // the same for the whole CTA (O1 is never written otherwise)
+        const float M = fmaxf(m_ref, x1.x);
+        // (exactly 1 for the slot holding the larger reference)
+        const float w0 = m_ref == -INFINITY ? 0.f : m_ref == M ? 1.f : fast_exp2(m_ref - M);
+        const float w1 = (!has1 || x1.x == -INFINITY) ? 0.f : x1.x == M ? 1.f : fast_exp2(x1.x - M);
+        const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / (w0 * lsum + w1 * x1.y);
+        const float a0 = w0 * inv, a1 = w1 * inv;
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi_e) * HD;
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO + cc * 32, o0);
+          if (has1) tmem_ld32(tO + HD + cc * 32, o1);
+          tmem_wait_ld();
+          if (qi_e < q_len) {
+#pragma unroll
+            for (int e8 = 0; e8 < 4; ++e8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int e = e8 * 8 + 2 * u;
+                float v0 = __uint_as_float(o0[e]) * a0, v1 = __uint_as_float(o0[e + 1]) * a0;
+                if (has1) {
+                  v0 = fmaf(__uint_as_float(o1[e]), a1, v0);
+                  v1 = fmaf(__uint_as_float(o1[e + 1]), a1, v1);
+                }
+                const __nv_bfloat162 pk = __floats2bfloat162_rn(v0, v1);
+                w[u] = *reinterpret_cast<const uint32_t*>(&pk);
+              }
+              reinterpret_cast<uint4*>(orow)[cc * 4 + e8] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    } else if (!SPLIT) {
       if (nkv > 0) {
-        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi_e) * HD;
         const float inv = *abort_flag ? __int_as_float(0x7fc00000) : 1.f / lsum;
 #pragma unroll
         for (int cc = 0; cc < HD / 32; ++cc) {  // 32 columns at a time keeps the register count down
           uint32_t o[32];
           tmem_ld32(tO + cc * 32, o);
           tmem_wait_ld();
-          if (qi < q_len) {
+          if (qi_e < q_len) {
 #pragma unroll
             for (int e8 = 0; e8 < 4; ++e8) {
               uint32_t w[4];
@@ -593,8 +709,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         dsmem_st4(ra + (HD / 4) * 512, make_float4(m_ref, lsum, 0.f, 0.f));
       }
       cluster_sync_all();  // every partial has arrived
-      if (warp % ks == rank && qi < q_len) {
-        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi) * HD;
+      if (warp % ks == rank && qi_e < q_len) {
+        __nv_bfloat16* const orow = p.o + ((size_t(b) * p.Hq + h) * p.q_pitch + qi_e) * HD;
         const int slot = warp / ks;
         float M = -INFINITY;
         for (int src = 0; src < ks; ++src) M = fmaxf(M, xbuf[xidx<HD>(src, slot, upr, HD / 4, lane)]);
@@ -656,6 +772,98 @@ bool make_map(CUtensorMap* map, const void* base, int hd, uint64_t rows, uint64_
   return encode_bf16_rows(map, base, uint64_t(hd), rows, row_pitch, heads, 64, 128);
 }
 
+// Work units of a launch with uniform lengths: the first pair run as single
+// query tiles (ilv_from) and the pairs scheduled before those (n_first).
+struct UnitPlan {
+  int ilv_from, n_first;
+};
+
+// KV tiles that query tile t of a head needs (uniform lengths).
+long tile_kv_tiles(long t, long q_len, long kv_len, bool causal) {
+  const long m = t * BM;
+  if (m >= q_len) return 0;
+  long n = (kv_len + BN - 1) / BN;
+  if (causal) n = std::min(n, (kv_len - q_len + std::min(m + BM - 1, q_len - 1)) / BN + 1);
+  return n;
+}
+
+// The pairs scheduled before the single tiles: those longer than every
+// single tile (so that the grid runs longest first).
+int pairs_first(int ilv_from, long n_tiles, long q_len, long kv_len, bool causal) {
+  long max_single = 0;
+  for (long t = 2L * ilv_from; t < n_tiles; ++t)
+    max_single = std::max(max_single, (tile_kv_tiles(t, q_len, kv_len, causal) + 1) / 2);
+  int n = 0;
+  for (long pr = ilv_from - 1; pr >= 0; --pr) {
+    const long it = std::max(tile_kv_tiles(2 * pr, q_len, kv_len, causal),
+                             tile_kv_tiles(2 * pr + 1, q_len, kv_len, causal));
+    if (it <= max_single) break;
+    ++n;
+  }
+  return n;
+}
+
+// Planner (D = 64): list-schedule the units of each candidate first
+// single-tile pair on the SMs in launch order and keep the shortest
+// makespan, ties going to pairs alone.  The costs, in iterations of the
+// pair-only kernel, were fitted to a sweep of every candidate at 513 to
+// 8192 causal queries (model against measurement within about 1 us): a
+// unit's set-up and epilogue 3.3, a two-tile iteration 1.0, and 1.074 for
+// every iteration of the kernel that holds single-tile units (its unit
+// bookkeeping costs the softmax loop registers).  Only causal grids of a
+// few waves can gain (the longest pairs bound them); the result is cached
+// per shape.  At D = 128 single tiles did not pay in any case measured.
+UnitPlan plan_units(long q_len, long kv_len, bool causal, long heads, int sms) {
+  const int n_pairs = int((q_len + 2 * BM - 1) / (2 * BM));
+  const long n_tiles = (q_len + BM - 1) / BM;
+  UnitPlan none{n_pairs, 0};
+  if (!causal || long(n_pairs) * heads > 16L * sms || n_tiles > 65535) return none;
+  static std::mutex mu;
+  static std::map<std::array<long, 5>, UnitPlan> cache;
+  const std::array<long, 5> key{q_len, kv_len, long(causal), heads, long(sms)};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  constexpr double kSetup = 3.3, kIlvKernel = 1.074;
+  std::vector<long> pair_it(n_pairs), single_it(n_tiles);
+  for (int pr = 0; pr < n_pairs; ++pr)
+    pair_it[pr] = std::max(tile_kv_tiles(2L * pr, q_len, kv_len, causal),
+                           tile_kv_tiles(2L * pr + 1, q_len, kv_len, causal));
+  for (long t = 0; t < n_tiles; ++t) single_it[t] = (tile_kv_tiles(t, q_len, kv_len, causal) + 1) / 2;
+  UnitPlan best = none;
+  double best_span = 0.0;
+  std::vector<double> sm_free;
+  for (int from = n_pairs; from >= 0; --from) {
+    const int n_first = pairs_first(from, n_tiles, q_len, kv_len, causal);
+    std::vector<long> order;  // unit costs in launch order (y), each for every head
+    for (int i = 0; i < n_first; ++i) order.push_back(pair_it[from - 1 - i]);
+    for (long t = n_tiles - 1; t >= 2L * from; --t) order.push_back(single_it[t]);
+    for (int pr = from - 1 - n_first; pr >= 0; --pr) order.push_back(pair_it[pr]);
+    const double per_it = from == n_pairs ? 1.0 : kIlvKernel;
+    sm_free.assign(size_t(sms), 0.0);
+    std::priority_queue<double, std::vector<double>, std::greater<double>> q(sm_free.begin(), sm_free.end());
+    double span = 0.0;
+    for (const long c : order)
+      for (long hh = 0; hh < heads; ++hh) {
+        const double start = q.top();
+        q.pop();
+        const double end = start + kSetup + per_it * double(c);
+        span = std::max(span, end);
+        q.push(end);
+      }
+    if (from == n_pairs || span < best_span - 1e-9) {
+      best_span = span;
+      best = UnitPlan{from, n_first};
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 1024) cache.clear();
+  cache[key] = best;
+  return best;
+}
+
 template <int HD>
 cudaError_t launch_prefill_hd(const PrefillArgs& a, cudaStream_t stream) {
   using C = PfCfg<HD>;
@@ -702,17 +910,33 @@ cudaError_t launch_prefill_hd(const PrefillArgs& a, cudaStream_t stream) {
     if (const int v = prefill_kv_split_override(); v >= 1 && v <= 8) ks = v;  // tuning and tests only
     while (!kv_split_fits(C::X_MAX_UNITS, ks)) --ks;
     p.kv_splits = ks;
+    // work units: pairs, and for the longest causal tiles single tiles
+    p.n_tiles = (a.q_len + BM - 1) / BM;
+    UnitPlan up{p.n_pairs, 0};
+    if (ks == 1 && !varlen) {
+      const int forced = prefill_interleave_override();  // tuning and tests only
+      if (forced >= 0) {
+        up.ilv_from = std::min(forced, p.n_pairs);
+        up.n_first = pairs_first(up.ilv_from, p.n_tiles, a.q_len, a.kv_len, a.causal != 0);
+      } else if (HD == 64) {
+        up = plan_units(a.q_len, a.kv_len, a.causal != 0, long(a.B) * a.Hq, sms);
+      }
+      if (std::max(0, p.n_tiles - 2 * up.ilv_from) + up.ilv_from > 65535) up = UnitPlan{p.n_pairs, 0};
+    }
+    p.ilv_from = up.ilv_from;
+    p.n_first = up.n_first;
   }
   static bool configured = false;
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    for (const void* k : {reinterpret_cast<const void*>(prefill_kernel<HD, false, false>),
+                          reinterpret_cast<const void*>(prefill_kernel<HD, true, false>),
+                          reinterpret_cast<const void*>(prefill_kernel<HD, false, true>)}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
     configured = true;
   }
-  const dim3 grid(a.B * a.Hq * p.kv_splits, p.n_pairs);
+  const dim3 grid(a.B * a.Hq * p.kv_splits, std::max(0, p.n_tiles - 2 * p.ilv_from) + p.ilv_from);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHR);
@@ -728,10 +952,12 @@ cudaError_t launch_prefill_hd(const PrefillArgs& a, cudaStream_t stream) {
   cfg.attrs = attr;
   if (p.kv_splits == 1) {
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, false>, tq, tk, tv, p);
+    if (p.n_tiles - 2 * p.ilv_from > 0)  // single-tile units in the grid
+      return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, false, true>, tq, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, false, false>, tq, tk, tv, p);
   }
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, true>, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, true, false>, tq, tk, tv, p);
 }
 
 }  // namespace

@@ -290,6 +290,19 @@ GQA_ATTN_API int gqa_attn_quantize_q4(const void* src, int64_t src_head_rows, ui
  * ------------------------------------------------------------------------- */
 GQA_ATTN_API int gqa_attn_set_plan_override(int decode_splits, int prefill_kv_split);
 
+/* Prefill work units, for tuning and tests only.  Prefill runs the 128-row
+ * query tiles of a head in pairs (two tiles over the same keys) and, for the
+ * longest causal tiles, one tile per CTA whose keys the CTA's two softmax
+ * warpgroups take in turn (halving the tile's iterations); the planner picks
+ * the first pair run that way.  from_pair >= 0 forces it: pairs from index
+ * from_pair on (pair p holds tiles 2p and 2p+1) run as single tiles, so 0
+ * makes every tile a single-tile unit and a value past the last pair turns
+ * them off.  A negative value restores the planner's choice (the initial
+ * setting).  Cluster-split prefill (see above) and per-request lengths
+ * always use pairs.  Same threading rules as gqa_attn_set_plan_override.
+ * Returns GQA_OK. */
+GQA_ATTN_API int gqa_attn_set_prefill_interleave_override(int from_pair);
+
 /* ---------------------------------------------------------------------------
  * Single-token decode without any caller-provided or allocated scratch.
  *

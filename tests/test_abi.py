@@ -102,6 +102,13 @@ def test_plan_override_checks_its_arguments(lib):
     assert lib.gqa_attn_set_plan_override(0, 0) == binding.GQA_OK
 
 
+def test_prefill_interleave_override_accepts_any_value_and_resets(lib):
+    for v in (0, 3, 1 << 20, -1, -7):
+        assert lib.gqa_attn_set_prefill_interleave_override(v) == binding.GQA_OK
+    with binding.plan_override(prefill_interleave_from=2):
+        pass  # restores the planner's choice on exit
+
+
 def test_plan_override_is_not_read_from_the_environment(lib, monkeypatch):
     """Only the explicit call changes a plan: the split count the planner
     reports does not move when a tuning-looking variable is set."""

@@ -135,6 +135,15 @@ def test_kv_split_over_cluster(ks, q_len, kv_len, causal):
         check_full(q, k, v, kv_len, causal)
 
 
+@pytest.mark.parametrize("from_pair", [0, 2])
+@pytest.mark.parametrize("q_len,kv_len,causal", [(129, 129, True), (513, 513, True), (100, 150, True),
+                                                  (300, 2000, False)])
+def test_single_tile_units(from_pair, q_len, kv_len, causal):
+    q, k, v = case(1, 28, 4, q_len, kv_len, layer=from_pair + 5)
+    with binding.plan_override(prefill_interleave_from=from_pair):
+        check_full(q, k, v, kv_len, causal)
+
+
 def test_back_to_back_calls_read_the_previous_output():
     q, k, v = case(1, 28, 4, 512, 4096, layer=11)
     _, k2, v2 = case(1, 28, 4, 512, 4096, layer=12)

@@ -132,6 +132,43 @@ def test_kv_split_over_cluster(ks, q_len, kv_len, causal):
         check_full(q, k, v, kv_len, causal)
 
 
+@pytest.mark.parametrize("from_pair", [0, 1, 2])
+@pytest.mark.parametrize("q_len,kv_len,causal", [(1, 1, True), (127, 127, True), (129, 129, True), (300, 300, True),
+                                                  (513, 513, True), (1000, 1000, True), (100, 150, True),
+                                                  (129, 1000, True), (300, 2000, False), (256, 256, False)])
+def test_single_tile_units(from_pair, q_len, kv_len, causal):
+    """Pairs from `from_pair` on run as single query tiles whose KV tiles the
+    two softmax warpgroups take in turn (forced through the tuning
+    override); chunks whose first rows see none of the odd KV tiles (100
+    queries at 150 keys) and tiles with one KV tile (no odd tiles) included."""
+    q, k, v = case(1, 14, 2, q_len, kv_len, layer=from_pair + 3)
+    with binding.plan_override(prefill_interleave_from=from_pair):
+        check_full(q, k, v, kv_len, causal)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_single_tile_units_rescale(causal):
+    """Growing key norms force rescales in both slots of single-tile units."""
+    T = 1000
+    q, k, v = case(1, 14, 2, T, T, layer=22)
+    ramp = (1.0 + 6.0 * torch.arange(T, device=DEV, dtype=torch.float32) / T).view(1, 1, T, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    with binding.plan_override(prefill_interleave_from=0):
+        check_full(q, k, v, T, causal)
+
+
+def test_single_tile_units_equal_pairs_bit_for_bit_where_slot_one_is_empty():
+    """A tile with a single KV tile gives slot 1 nothing to do: its single-tile
+    unit must then reproduce the pair result exactly (same products, same
+    order, weight 1 for slot 0)."""
+    q, k, v = case(1, 14, 2, 100, 100, layer=9)
+    o_pair = binding.prefill(q, k, v)
+    with binding.plan_override(prefill_interleave_from=0):
+        o_single = binding.prefill(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o_pair, o_single)
+
+
 @pytest.mark.parametrize("q_len,kv_len", [(300, 300), (512, 4096)])
 def test_back_to_back_calls_read_the_previous_output(q_len, kv_len):
     """Launches wait for the grid before them (programmatic dependent launch):

@@ -74,12 +74,16 @@ def test_varlen_head_mappings(Hq, Hkv):
 
 
 def test_varlen_uniform_equals_plain_prefill():
-    """Equal lengths for every request: the same as gqa_attn_prefill."""
+    """Equal lengths for every request: the same as gqa_attn_prefill run with
+    pairs of query tiles only (per-request lengths always use pairs; the
+    plain call's planner may run long causal tiles as single-tile units,
+    which sum the same products in another order)."""
     B, q_len, kv_len = 3, 300, 900
     q = inputs.randn((B, 14, q_len, 64), 7, torch.bfloat16, DEV)
     k = inputs.randn((B, 2, kv_len, 64), 8, torch.bfloat16, DEV)
     v = inputs.randn((B, 2, kv_len, 64), 9, torch.bfloat16, DEV)
-    o1 = binding.prefill(q, k, v, causal=True)
+    with binding.plan_override(prefill_interleave_from=1 << 20):
+        o1 = binding.prefill(q, k, v, causal=True)
     o2 = torch.empty_like(q)
     lens = lambda n: torch.full((B,), n, dtype=torch.int32, device=DEV)
     binding.gqa_attn_prefill_varlen(q, k, v, o2, lens(q_len), lens(kv_len), 0.125)
