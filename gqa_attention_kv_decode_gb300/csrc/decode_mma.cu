@@ -157,15 +157,16 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
 
   // Launched early (programmatic dependent launch): until the wait returns,
   // only prefetch the first tiles of this split into L2 (as if kv_len were
-  // max_kv_len) and the tensor maps.  All NSTAGE tiles for the 8-warp shape
-  // (one long request: 28-call sequences at 32,768 keys 14.7 us per call,
-  // 15.4 with one tile), one for the 4-warp shape, where more competes for
-  // HBM with the previous call's last CTAs (Qwen3-4B ragged B = 64: 164.7
-  // against 169.8 us per call).
+  // max_kv_len) and the tensor maps.  Two tiles for the 8-warp shape (one
+  // long request; 28-call sequences at 32,768 keys in a CUDA graph: 14.5 us
+  // per call, 14.8 with all three stages, 15.3 with five tiles; plain
+  // launches 14.8 with two or three, 15.4 with one), one for the 4-warp
+  // shape, where more competes for HBM with the previous call's last CTAs
+  // (Qwen3-4B ragged B = 64: 166.0 against 171.3 us per call).
   if (tid == 0 && hc == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    constexpr int kPrefetchTiles = NW == 8 ? NSTAGE : 1;
+    constexpr int kPrefetchTiles = NW == 8 ? 2 : 1;
     for (int t = 0; t < (PAGED ? 0 : kPrefetchTiles); ++t) {  // (a paged cache's rows are known only after the wait)
       const int row0 = (split + t * p.n_split) * TILE;
       if (row0 >= p.max_kv_len) break;
