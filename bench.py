@@ -952,6 +952,15 @@ def main():
         for _ in range(args.warmup):
             time_decode_step(binding, layers, outs, ws, S, stream)
     torch.cuda.synchronize()
+    # The step as a decode step is run in production: its 28 calls (made
+    # through the public API) captured once in a CUDA graph and replayed.
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph, stream=stream):
+        time_decode_step(binding, layers, outs, ws, S, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step_graph.replay()
+    torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -962,12 +971,24 @@ def main():
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for _ in range(args.steps):
-            time_decode_step(binding, layers, outs, ws, S, stream)
+            step_graph.replay()
         t_end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     elapsed_ms = dist.max(t_start.elapsed_time(t_end))
     ms_per_step = elapsed_ms / args.steps
+
+    # the same K steps as plain launches (the 28 calls issued one by one)
+    l_start = torch.cuda.Event(enable_timing=True)
+    l_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        l_start.record(stream)
+        for _ in range(args.steps):
+            time_decode_step(binding, layers, outs, ws, S, stream)
+        l_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    launch_ms_per_step = dist.max(l_start.elapsed_time(l_end)) / args.steps
 
     # the spread of the step times, from K more steps with an event at every
     # step boundary (outside the region above, which has none)
@@ -1060,13 +1081,17 @@ def main():
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": S,
                    "layers_per_step": LAYERS, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (3.76 GB per step on distinct buffers); no flush needed"},
+                   "l2": "inputs larger than L2 (3.76 GB per step on distinct buffers); no flush needed",
+                   "launch": "the step's 28 public-API calls captured once in a CUDA graph, replayed K times"},
+        "plain_launches": {"value": round(replica_value(world, step_bytes, launch_ms_per_step), 1), "unit": "GB/s",
+                           "ms_per_step": round(launch_ms_per_step, 4),
+                           "note": "the same K steps with the 28 calls issued one by one"},
         "hbm_fraction": round(value / world / hbm_peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "kernel": "decode_split_kernel<float,128,7,2,3> + decode_merge_kernel",
                      "peak_source": peak_src, "avg_launch_us": round(avg_launch_us, 3),
-                     "timing": "events on the launching stream around the K timed steps / (K x 28 calls)",
+                     "timing": "events on the launching stream around the K timed graph replays / (K x 28 calls)",
                      "isolated_call_us": round(isolated_call_us, 3),
                      "basis": "per-call stream average: consecutive calls overlap (each split kernel "
                               "is launched early and prefetches into L2 while the previous merge runs)",
