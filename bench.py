@@ -843,20 +843,20 @@ def _case_inputs(name, device):
         # prefill-T4097, prefill-q512-kv4096 (Qwen2.5-0.5B heads, D=64) or
         # prefill-d128-T4097 (Qwen2.5-7B heads, D=128)
         parts = name.split("-")[1:]
-        Hq, Hkv, D = 14, 2, 64
+        hq, hkv, hd = 14, 2, 64
         if parts[0] == "d128":
-            Hq, Hkv, D = 28, 4, 128
+            hq, hkv, hd = 28, 4, 128
             parts = parts[1:]
         if len(parts) == 1:
             q_len = kv_len = int(parts[0][1:])
         else:
             q_len, kv_len = int(parts[0][1:]), int(parts[1][2:])
-        q = inputs.randn((1, Hq, q_len, D), inputs.tensor_seed(0, 0), torch.bfloat16, device)
-        k = inputs.randn((1, Hkv, kv_len, D), inputs.tensor_seed(0, 1), torch.bfloat16, device)
-        v = inputs.randn((1, Hkv, kv_len, D), inputs.tensor_seed(0, 2), torch.bfloat16, device)
+        q = inputs.randn((1, hq, q_len, hd), inputs.tensor_seed(0, 0), torch.bfloat16, device)
+        k = inputs.randn((1, hkv, kv_len, hd), inputs.tensor_seed(0, 1), torch.bfloat16, device)
+        v = inputs.randn((1, hkv, kv_len, hd), inputs.tensor_seed(0, 2), torch.bfloat16, device)
         o = torch.empty_like(q)
-        flops = metrics.prefill_flops(Hq, D, q_len, kv_len, causal=True)
-        return (lambda st: binding_mod().gqa_attn_prefill(q, k, v, o, kv_len, D ** -0.5, True, st)), flops, "flop"
+        flops = metrics.prefill_flops(hq, hd, q_len, kv_len, causal=True)
+        return (lambda st: binding_mod().gqa_attn_prefill(q, k, v, o, kv_len, hd ** -0.5, True, st)), flops, "flop"
     raise SystemExit(f"unknown kernel case {name!r}")
 
 

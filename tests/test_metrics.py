@@ -49,3 +49,20 @@ def test_quantize_bytes_per_row():
     # fp16 (scale, bias) pairs: 256 + 64 + 8
     assert metrics.quantize_bytes(1, 128) == 328
     assert metrics.quantize_bytes(10, 64) == 10 * (128 + 32 + 4)
+
+
+def test_bench_kernel_cases_do_not_shadow_the_workload_constants():
+    """`bench.py --kernel CASE` builds its inputs in one function; a local
+    name equal to a module constant (D, HQ, ...) makes that constant local to
+    the whole function and breaks the other cases at run time."""
+    import symtable
+
+    import bench
+
+    src = open(bench.__file__).read()
+    top = symtable.symtable(src, bench.__file__, "exec")
+    fn = next(c for c in top.get_children() if c.get_name() == "_case_inputs")
+    constants = {"D", "HQ", "HKV", "S_HEAD", "LAYERS", "PREFILL_LAYERS"}
+    assert not (constants & set(fn.get_locals())), constants & set(fn.get_locals())
+    for case in bench.KERNEL_CASES:
+        assert case.split("-")[0] in {"decode", "q4", "quantize", "prefill", "varlen"}
