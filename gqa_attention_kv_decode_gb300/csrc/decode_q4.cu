@@ -1,6 +1,6 @@
 // decode_q4.cu -- single-token GQA decode over a 4-bit group-affine KV cache,
 // dequantised inside the attention loop, with both products on the tensor
-// cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation; sm_103a).
+// cores (mma.sync m16n8k16, fp32 accumulation; sm_103a).
 //
 // The cache stores, per (request, KV head, token), D/2 bytes of 4-bit codes
 // (element 2t in the low nibble of byte t) and one fp16 scale and bias per
@@ -13,21 +13,23 @@
 //   sum_j p_j v_j = sum_j (p_j s_jg) c_j + sum_j p_j b_jg
 // so the tensor cores only ever see the integer codes.
 //
-// A code c enters an MMA as the bf16 value 128 + c (bit pattern 0x4300 | c,
-// exact): one byte permute or shift and one mask per pair of codes.  The
-// offset is removed exactly: on the K side with the per-group sum of q
-// (sum q_i (128 + c_i) - 128 sum q_i), on the V side with one extra MMA whose
-// A operand is the constant 128.
-//
-//   S = Q K^T     M = query heads: rows 0-7 hold q over the dims of group 0,
-//                 rows 8-15 q over group 1, so one accumulator keeps both
-//                 groups' partial sums apart; N = 8 keys; K = 16 dims.  The
-//                 k index is a permutation of the dims chosen so that a
-//                 thread's 4 codes of a k-step come from 2 bytes of one word.
-//   O^T = V^T P^T M = 16 dims (a permutation within one group), N = 8 query
-//                 heads, K = 16 keys.  The B operand (p_j s_jg, bf16) comes
-//                 straight from the score accumulators: their layout (head =
-//                 row group, keys = column pairs) is the B-fragment layout.
+//   S^T = K Q^T   fp16: M = the warp's 16 keys, N = 8 query heads, K = 16
+//                 dims.  A code enters as an exact fp16 value: the nibble in
+//                 bits 0-3 of a half-word under the exponent of 1024 gives
+//                 1024 + c, the nibble in bits 4-7 under the exponent of 64
+//                 gives 64 + c (one mask-and-or per pair of codes, one shift
+//                 per word).  The k index is a permutation of the dims that
+//                 puts a thread's 4 codes of a k-step in 2 bytes of one
+//                 word.  q is scaled by 2^-e (exact, e per CTA) to stay below
+//                 2^14 in fp16; the offsets are removed with the per-group
+//                 sums of q (1024 sum_even q + 64 sum_odd q).
+//   O^T = V^T P^T bf16: M = 16 dims of one group, N = 8 query heads, K = 16
+//                 keys.  A code enters as the bf16 value 128 + c (a byte
+//                 permute, a shift and a mask per pair); the offset is removed
+//                 by one extra MMA per group whose A operand is the constant
+//                 128.  The B operand p_j s_jg (bf16, for range) is built in
+//                 the layout of the score accumulators and transposed to the
+//                 B-fragment layout with movmatrix.
 //
 // The CTA structure is the one of the other decode kernels: 4 warps, tiles of
 // 64 keys (warp w takes keys 16w..16w+15), tiles dealt round-robin to the
