@@ -155,8 +155,12 @@ class ClockSampler:
 
 
 def kernel_source_hash(name):
-    with open(os.path.join(ROOT, "gqa_attention_kv_decode_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel source with its // comments and blank lines left out,
+    so that a comment edit does not retire an ncu record of unchanged code."""
+    with open(os.path.join(ROOT, "gqa_attention_kv_decode_gb300", "csrc", name)) as f:
+        lines = (line.split("//", 1)[0].rstrip() for line in f)
+        code = "\n".join(line for line in lines if line)
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def recorded_ncu(kernel_file, key):

@@ -1,4 +1,5 @@
-// decode.cu -- split-KV single-token GQA decode for sm_103a (fp32 / bf16 KV).
+// decode.cu -- split-KV single-token GQA decode for sm_103a on the CUDA cores
+// (fp32 KV caches; bf16 caches run on the tensor cores, decode_mma.cu).
 //
 // One CTA serves one (request b, KV head g, query-head chunk, key split).  All
 // the query heads that share KV head g (n_rep = Hq / Hkv of them, up to 8 per

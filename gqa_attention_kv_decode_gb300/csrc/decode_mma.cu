@@ -12,9 +12,10 @@
 //   O += P V    P taken straight from the score accumulators (their layout
 //               is the A-operand layout of the next product), V fragments
 //               read with ldmatrix.trans.
-// The CTA structure is the one of the CUDA-core kernel: 4 warps, tiles of 64
-// keys (warp w takes keys 16w..16w+15 of every tile), tiles dealt round-robin
-// to the splits, a per-warp online softmax in base 2, warps merged in shared
+// The CTA structure is the one of the CUDA-core kernel: 4 warps and tiles of
+// 64 keys (or, for one long request, 8 warps and tiles of 128 keys), warp w
+// taking keys 16w..16w+15 of every tile, tiles dealt round-robin to the
+// splits, a per-warp online softmax in base 2, warps merged in shared
 // memory, and split partials merged by the shared merge kernel.  K and V
 // tiles arrive by tiled TMA with 128-byte swizzle (rows of 128 bytes, 16-byte
 // chunks XOR-ed with the row index), so the 8 rows an ldmatrix reads sit in 8
