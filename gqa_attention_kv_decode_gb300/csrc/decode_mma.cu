@@ -178,6 +178,12 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
   }
   if (tid == 32)  // and this CTA's query rows
     prefetch_l2_bulk(p.q + (size_t(b) * p.Hq + h0) * D, uint32_t(nh * D * 2));
+  // The 8-warp shape (one long request) lets the merge kernel's CTAs be
+  // scheduled at once; they wait for this grid anyway, and being resident
+  // when it ends shortens the hand-off (32,768 keys in a CUDA graph: 14.30
+  // against 14.52 us per call; the 4-warp shape, ragged batches, measured
+  // slower that way and triggers near its end, below).
+  if constexpr (NW == 8) grid_launch_dependents();
   grid_dependency_wait();
 
   int L = p.kv_lens ? p.kv_lens[p.kv_period > 0 ? b % p.kv_period : b] : p.max_kv_len;
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
   }
   __syncthreads();
   // let the merge kernel's CTAs be scheduled while this grid drains
-  grid_launch_dependents();
+  if constexpr (NW != 8) grid_launch_dependents();
 
   // ---- merge the warps, then write O or this split's partial ----
   const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
