@@ -59,6 +59,9 @@ struct DecodeParams {
   const void* k_new;  // [B][Hkv][D]: token appended at row kv_lens[b] - 1, or null
   const void* v_new;
   int kv_period;  // > 0: layers stacked along the batch axis share kv_lens[b % kv_period]
+  // call boundary (see the kernel): 1 for a long context with few units --
+  // trigger the merge's launch at the start and start two tiles towards L2
+  int long_few;
 };
 
 
@@ -104,7 +107,9 @@ struct Cfg {
 // (a multiple of which the block size is) never crosses a block.  With k_new
 // the CTA that owns row kv_len - 1 writes the new token into its tile in
 // shared memory and into the pool.
-constexpr int kPrefetchTiles = 1;  // tiles of a split started towards L2 before the dependency wait
+// A long context with few (request, KV head) units: the call-boundary
+// settings of decode_split_kernel for it (see there).
+constexpr int kLongFewUnits = 16, kLongFewKeys = 8192;
 
 template <typename T, int D, int NREP, int R_, int NSTAGE, bool PAGED>
 __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
@@ -133,9 +138,14 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   // not NSTAGE: more competes for HBM with the previous call's last CTAs,
   // which are on the critical path (28-call sequences at 32,768 keys: 26.4
   // against 26.5 us per call with plain launches, 25.9 against 27.7 in a
-  // CUDA graph; no prefetch: 27.4 / 26.9).
+  // CUDA graph; no prefetch: 27.4 / 26.9).  A long context with few units
+  // (p.long_few) prefetches two tiles and lets the merge kernel's CTAs be
+  // scheduled at once, so that they are resident when this grid ends:
+  // 32,768 keys 25.6 / 26.3 us (graph / plain launches), 8192 keys 11.3 /
+  // 12.0 against 11.8 / 12.2; at 128 and 2048 keys that measured slower.
+  if (p.long_few) grid_launch_dependents();
   if (!PAGED && tid == 0 && hc == 0) {  // (a paged cache's rows are known only after the wait)
-    for (int t = 0; t < kPrefetchTiles; ++t) {
+    for (int t = 0; t < (p.long_few ? 2 : 1); ++t) {
       const int row0 = (split + t * p.n_split) * TILE;
       if (row0 >= p.max_kv_len) break;
       const uint32_t bytes = uint32_t(min(TILE, p.max_kv_len - row0)) * C::ROWB;
@@ -497,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   }
   __syncthreads();
   // let the merge kernel's CTAs be scheduled while this grid drains
-  grid_launch_dependents();
+  if (!p.long_few) grid_launch_dependents();
 
   // ---- merge the consumer warps, then write O or this split's partial ----
   const size_t ws_row = size_t(b) * p.Hq + h0;  // first query head of this CTA
@@ -614,6 +624,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.k_new = a.k_new;
   p.v_new = a.v_new;
   p.kv_period = a.kv_period;
+  p.long_few = (a.block_table == nullptr && long(a.B) * a.Hkv * a.plan.n_hc <= kLongFewUnits &&
+                a.max_kv_len >= kLongFewKeys) ? 1 : 0;
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   cudaError_t e;
   if (a.dtype != GQA_F32)
