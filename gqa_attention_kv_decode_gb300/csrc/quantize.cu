@@ -25,11 +25,15 @@
 // quotient a correctly rounded fp32 division returns, and the ties of
 // round-half-even are decided on the same value.
 //
-// A lane loads 16 bytes (8 elements); D/8 lanes hold a row and 8 lanes a
-// group, whose minimum and maximum come from three xor shuffles.  A warp keeps
-// UNR = 4 such loads in flight (8 rows at D = 128) before it computes.  Codes are
-// written as 4 bytes per lane (one contiguous D/2-byte run per row), the
-// group's scale and bias by its first lane.  HBM-bound: 2D bytes read,
+// A lane holds 32 elements (four 16-byte loads of one row); D/32 lanes hold a
+// row and 2 lanes a group, whose minimum and maximum come from one xor
+// shuffle.  The per-group work (the scale's division, the reciprocal, the
+// fp16 roundings) is one instruction stream for all lanes of a warp, so more
+// elements per lane divide its cost: a 16,384-token cache at B = 4, Hkv = 8
+// took 43.7 us with 8 elements a lane and 37.5 us with 16 or 32; a 64-token
+// flush 6.7 us with 16 and 6.1 with 32.  Codes are written as 16 bytes per
+// lane (one contiguous D/2-byte run per row), the group's scale and bias by
+// its first lane.  HBM-bound: 2D bytes read,
 // D/2 + 4 D/64 written per row.  The grid is (row blocks, heads), so no lane
 // divides to find its head.
 #include <cuda_bf16.h>
@@ -42,6 +46,8 @@
 namespace gqa {
 namespace {
 
+constexpr int kQuantEpl = 32;  // elements a lane quantizes (16 or 32)
+
 struct QuantParams {
   const __nv_bfloat16* src;
   uint8_t* codes;
@@ -53,15 +59,21 @@ struct QuantParams {
 
 template <int D>
 struct QuantCfg {
-  static constexpr int LPR = D / 8;     // lanes per row (8 elements a lane)
-  static constexpr int RPL = 32 / LPR;  // rows per warp-wide load
-  static constexpr int UNR = 4;         // loads in flight per lane
+  static constexpr int EPL = kQuantEpl;  // elements a lane holds
+  static constexpr int NV = EPL / 8;     // 16-byte loads per lane and row
+  static constexpr int LPR = D / EPL;    // lanes per row
+  static constexpr int LPG = 64 / EPL;   // lanes per group
+  static constexpr int RPL = 32 / LPR;   // rows per warp-wide load
+  static constexpr int UNR = 32 / EPL;   // rows in flight per lane (64 bytes)
   static constexpr int ROWS_PER_CTA = 8 * RPL * UNR;  // 8 warps
 };
 
 template <int D>
 __global__ void __launch_bounds__(256) quantize_q4_kernel(const QuantParams p) {
+  constexpr int EPL = QuantCfg<D>::EPL;
+  constexpr int NV = QuantCfg<D>::NV;
   constexpr int LPR = QuantCfg<D>::LPR;
+  constexpr int LPG = QuantCfg<D>::LPG;
   constexpr int RPL = QuantCfg<D>::RPL;
   constexpr int UNR = QuantCfg<D>::UNR;
   constexpr int NG = D / 64;          // groups per row
@@ -73,30 +85,41 @@ __global__ void __launch_bounds__(256) quantize_q4_kernel(const QuantParams p) {
   const long long head = blockIdx.y + (long long)gridDim.y * blockIdx.z;
   if (head >= p.heads) return;
   const int row0 = (int(blockIdx.x) * 8 + (int(threadIdx.x) >> 5)) * (RPL * UNR);
-  const int col = lane % LPR;         // 8-element chunk of the row
-  const __nv_bfloat16* src = p.src + head * p.src_head_rows * D + col * 8;
+  const int col = lane % LPR;         // 16-element chunk of the row
+  const __nv_bfloat16* src = p.src + head * p.src_head_rows * D + col * EPL;
   const long long dst0 = head * p.dst_head_rows + p.dst_row0;
-  uint4 w[UNR];
+  uint4 w[UNR][NV];
   int rows[UNR];
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
     rows[u] = row0 + u * RPL + lane / LPR;
-    w[u] = rows[u] < p.rows ? *reinterpret_cast<const uint4*>(src + (long long)rows[u] * D)
-                            : make_uint4(0u, 0u, 0u, 0u);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + (long long)rows[u] * D);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) w[u][k] = rows[u] < p.rows ? s4[k] : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
-    const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+    uint32_t ww[EPL / 2];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      ww[4 * k] = w[u][k].x;
+      ww[4 * k + 1] = w[u][k].y;
+      ww[4 * k + 2] = w[u][k].z;
+      ww[4 * k + 3] = w[u][k].w;
+    }
     // group minimum and maximum on the bf16 pairs (exact), carried through the
     // shuffles as one (min, -max) pair
-    __nv_bfloat162 bw[4];
+    __nv_bfloat162 mn = *reinterpret_cast<const __nv_bfloat162*>(&ww[0]), mx = mn;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) bw[i] = *reinterpret_cast<const __nv_bfloat162*>(&ww[i]);
-    const __nv_bfloat162 mn = __hmin2(__hmin2(bw[0], bw[1]), __hmin2(bw[2], bw[3]));
-    const __nv_bfloat162 nmx = __hneg2(__hmax2(__hmax2(bw[0], bw[1]), __hmax2(bw[2], bw[3])));
+    for (int i = 1; i < EPL / 2; ++i) {
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&ww[i]);
+      mn = __hmin2(mn, x);
+      mx = __hmax2(mx, x);
+    }
+    const __nv_bfloat162 nmx = __hneg2(mx);
     __nv_bfloat162 v = __hmin2(__lows2bfloat162(mn, nmx), __highs2bfloat162(mn, nmx));  // (lo, -hi)
 #pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {  // the 8 lanes of a group
+    for (int m = 1; m < LPG; m <<= 1) {  // the lanes of a group
       const uint32_t o = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<const uint32_t*>(&v), m);
       v = __hmin2(v, *reinterpret_cast<const __nv_bfloat162*>(&o));
     }
@@ -114,21 +137,24 @@ __global__ void __launch_bounds__(256) quantize_q4_kernel(const QuantParams p) {
     // above, rounded to the nearest integer, ties to even, by the saturating
     // conversion (negative values and NaN give 0), then capped at 15
     const float2 nb = make_float2(-bb, -bb), r2 = make_float2(rcp, rcp), ns2 = make_float2(-s, -s);
-    uint32_t packed = 0;
+    uint32_t packed[EPL / 8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int k = 0; k < EPL / 8; ++k) packed[k] = 0u;
+#pragma unroll
+    for (int i = 0; i < EPL / 2; ++i) {
       const float2 d = __fadd2_rn(bf16x2_to_float2(ww[i]), nb);
       float2 t = __fmul2_rn(d, r2);
       if (corr) t = __ffma2_rn(__ffma2_rn(t, ns2, d), r2, t);
       const uint32_t k0 = min(__float2uint_rn(t.x), 15u), k1 = min(__float2uint_rn(t.y), 15u);
-      packed += (k0 + 16u * k1) << (8 * i);
+      packed[i / 4] += (k0 + 16u * k1) << (8 * (i % 4));
     }
-    if (!(s > 0.f)) packed = 0u;
     const long long drow = dst0 + rows[u];
-    *reinterpret_cast<uint32_t*>(p.codes + drow * (D / 2) + col * 4) = packed;
-    if ((col & 7) == 0) {
-      p.scale[drow * NG + col / 8] = s16;
-      p.bias[drow * NG + col / 8] = b16;
+    uint32_t* cdst = reinterpret_cast<uint32_t*>(p.codes + drow * (D / 2) + col * (EPL / 2));  // (4-byte aligned)
+#pragma unroll
+    for (int k = 0; k < EPL / 8; ++k) cdst[k] = (s > 0.f) ? packed[k] : 0u;
+    if ((col % LPG) == 0) {
+      p.scale[drow * NG + col / LPG] = s16;
+      p.bias[drow * NG + col / LPG] = b16;
     }
   }
 }
