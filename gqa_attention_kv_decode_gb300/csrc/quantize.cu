@@ -31,9 +31,11 @@
 // fp16 roundings) is one instruction stream for all lanes of a warp, so more
 // elements per lane divide its cost: a 16,384-token cache at B = 4, Hkv = 8
 // took 43.7 us with 8 elements a lane and 37.5 us with 16 or 32; a 64-token
-// flush 6.7 us with 16 and 6.1 with 32.  Codes are written as 16 bytes per
-// lane (one contiguous D/2-byte run per row), the group's scale and bias by
-// its first lane.  HBM-bound: 2D bytes read,
+// flush 6.7 us with 16 and 6.1 with 32.  A lane keeps two rows (128 bytes)
+// in flight before it computes: 35.5 us (one row 37.6, four 37.5, the
+// registers then limiting the CTAs per SM).  Codes are written as 16 bytes
+// per lane (one contiguous D/2-byte run per row), the group's scale and bias
+// by its first lane.  HBM-bound: 2D bytes read,
 // D/2 + 4 D/64 written per row.  The grid is (row blocks, heads), so no lane
 // divides to find its head.
 #include <cuda_bf16.h>
@@ -64,7 +66,7 @@ struct QuantCfg {
   static constexpr int LPR = D / EPL;    // lanes per row
   static constexpr int LPG = 64 / EPL;   // lanes per group
   static constexpr int RPL = 32 / LPR;   // rows per warp-wide load
-  static constexpr int UNR = 32 / EPL;   // rows in flight per lane (64 bytes)
+  static constexpr int UNR = 64 / EPL;   // rows in flight per lane (128 bytes)
   static constexpr int ROWS_PER_CTA = 8 * RPL * UNR;  // 8 warps
 };
 
