@@ -604,13 +604,13 @@ ORACLE_SAMPLE = ("one KV head group (7 query heads, 1 of 4) of one layer call at
 ORACLE_SAMPLES = {
     "decode": ORACLE_SAMPLE,
     "prefill": ("causal prefill at Qwen2.5-0.5B head geometry, T=16384, bf16 inputs widened to fp64: "
-                "the last 128 query rows of one query head (each sees about 16,300 keys); "
+                "the last 512 query rows of one query head (each sees about 16,100 keys); "
                 "TFLOP/s from that sample's visible (query, key) pairs, 4*D flops each"),
     "q4": ("4-bit decode at Qwen3-4B head geometry, kv_len=16384: one request's KV head group "
            "(4 query heads, 1 of 8 heads x 4 requests), codes dequantised in fp64 then attended; "
            "GB/s scaled by that sample's algorithmic bytes (codes, scales, biases, q, o)"),
 }
-PF_T, PF_ROWS = 16384, 128
+PF_T, PF_ROWS = 16384, 512
 Q4_S = 16384
 
 
