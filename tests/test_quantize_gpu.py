@@ -34,14 +34,23 @@ def empty_cache(B, Hkv, S_cap, D, fill=0xA5):
     return codes, scale, bias
 
 
+def _same_fp16_bits(got, want):
+    """Equal fp16 bit patterns, except that a NaN matches any NaN (the
+    quantizer fixes no NaN payload: numpy's division and CUDA's conversion
+    write different quiet NaNs)."""
+    g = got.cpu().numpy()
+    gb, wb = g.view(np.int16), want.view(np.int16)
+    gn, wn = np.isnan(g), np.isnan(want)
+    np.testing.assert_array_equal(gn, wn)
+    np.testing.assert_array_equal(np.where(gn, 0, gb), np.where(wn, 0, wb))
+
+
 def check_rows(src, codes, scale, bias, dst_row0):
     n = src.shape[2]
     c, s, b = oracle.quantize_q4(src.float().cpu().numpy())
     np.testing.assert_array_equal(codes[:, :, dst_row0:dst_row0 + n].cpu().numpy(), c)
-    np.testing.assert_array_equal(scale[:, :, dst_row0:dst_row0 + n].cpu().view(torch.int16).numpy(),
-                                  torch.from_numpy(s).view(torch.int16).numpy())
-    np.testing.assert_array_equal(bias[:, :, dst_row0:dst_row0 + n].cpu().view(torch.int16).numpy(),
-                                  torch.from_numpy(b).view(torch.int16).numpy())
+    _same_fp16_bits(scale[:, :, dst_row0:dst_row0 + n], s)
+    _same_fp16_bits(bias[:, :, dst_row0:dst_row0 + n], b)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -166,3 +175,59 @@ def test_quantizer_ties_bit_for_bit():
     alt = np.clip(np.rint((x - b32) * (np.float32(1.0) / s32)), 0, 15).astype(np.uint8)
     alt = alt[:, 0::2] | (alt[:, 1::2] << 4)
     assert (alt != c).any()
+
+
+def _special_group(kind, rng):
+    """64 values of one group of a given kind (float32, exact in bf16 after
+    the caller's rounding).  Kinds 0, 12 and 13 are ordinary groups; the
+    others reach the clamps and the special values of the quantizer."""
+    x = rng.standard_normal(64).astype(np.float32)
+    if kind == 1:
+        x[rng.integers(64)] = np.nan                   # one NaN element: code 0, left out of min/max
+    elif kind == 2:
+        x[:] = np.nan                                  # all NaN: NaN scale and bias, codes 0
+    elif kind == 3:
+        x[rng.integers(64)] = np.inf                   # infinite maximum: infinite scale
+    elif kind == 4:
+        x[rng.integers(64)] = -np.inf                  # infinite minimum and bias
+    elif kind == 5:
+        x = np.float32(1e-4) * (1 + rng.integers(0, 8, 64).astype(np.float32) / 128)  # subnormal fp16 scale
+    elif kind == 6:
+        x = rng.uniform(0, 1, 64).astype(np.float32)
+        x[rng.integers(64)] = np.float32(-1e-6)        # fp16(min) != min: some x - bias < 0
+    elif kind == 7:
+        x = x * np.float32(1e5)                        # |min| past the fp16 range: infinite bias
+    elif kind == 8:
+        x = rng.uniform(0, 2e6, 64).astype(np.float32)  # range / 15 past the fp16 range
+    elif kind == 9:
+        x[:] = np.float32(0.75)                        # constant: zero scale
+    elif kind == 10:
+        x = np.where(rng.random(64) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+    elif kind == 11:
+        x[:] = np.nan
+        x[rng.integers(64)] = np.float32(2.5)          # one finite value: zero scale
+    elif kind == 12:
+        x = x - np.float32(5.0)
+    elif kind == 13:
+        x = x * np.float32(1e-3)
+    return x
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_quantizer_special_groups_bit_for_bit(D):
+    """Special groups (NaN elements, infinities, subnormal fp16 scales, a bias
+    that is not the minimum, zero scales) spread over the first 64 rows, so
+    that warps mix them with ordinary groups, and ordinary groups alone in
+    the rows after them: both code paths of the kernel against the oracle."""
+    rng = np.random.default_rng(2026 + D)
+    G, S = D // 64, 160
+    x = np.empty((S, D), dtype=np.float32)
+    for r in range(S):
+        for g in range(G):
+            kind = (r * G + g) % 14 if r < 64 else int(rng.choice([0, 12, 13]))
+            x[r, g * 64:(g + 1) * 64] = _special_group(kind, rng)
+    xb = torch.from_numpy(x).to(torch.bfloat16).view(1, 1, S, D).to(DEV)
+    codes, scale, bias = empty_cache(1, 1, S, D)
+    binding.gqa_attn_quantize_q4(xb, codes, scale, bias)
+    torch.cuda.synchronize()
+    check_rows(xb, codes, scale, bias, 0)
