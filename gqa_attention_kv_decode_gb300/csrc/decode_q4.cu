@@ -25,11 +25,17 @@
 //                 sums of q (1024 sum_even q + 64 sum_odd q).
 //   O^T = V^T P^T bf16: M = 16 dims of one group, N = 8 query heads, K = 16
 //                 keys.  A code enters as the bf16 value 128 + c (a byte
-//                 permute, a shift and a mask per pair); the offset is removed
-//                 by one extra MMA per group whose A operand is the constant
-//                 128.  The B operand p_j s_jg (bf16, for range) is built in
-//                 the layout of the score accumulators and transposed to the
-//                 B-fragment layout with movmatrix.
+//                 permute, a shift and a mask per pair).  The B operand
+//                 p_j s_jg (bf16, for range) is built in the layout of the
+//                 score accumulators and transposed to the B-fragment layout
+//                 with movmatrix.  Its rounding (2^-9 of each weight) is
+//                 multiplied by the code, so the codes are centred: one extra
+//                 MMA per group whose A operand is the constant 136 leaves
+//                 sum_j (c_j - 8) B_j, and the bias sums take
+//                 p_j (b_jg + 8 s_jg) with p_j s_jg before its rounding.
+//                 That halves the worst case (|c - 8| <= 8 against c <= 15):
+//                 a head whose weight sits on a few keys came 2.7e-2 off the
+//                 oracle before.
 //
 // The CTA structure is the one of the other decode kernels: 4 warps, tiles of
 // 64 keys (warp w takes keys 16w..16w+15), tiles dealt round-robin to the
@@ -149,6 +155,7 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
 // 1024 the nibble at bits 0-3 gives 1024 + c, and under the exponent of 64
 // the nibble at bits 4-7 gives 64 + c (its mantissa is 16c, scaled by 2^-4).
 constexpr uint32_t kBf128x2 = 0x43004300u;
+constexpr uint32_t kBf136x2 = 0x43084308u;  // 136 = 128 + 8: the centre of the codes above the offset
 __device__ __forceinline__ uint32_t nib_lo_bf16(uint32_t w) { return (w & 0x000F000Fu) | kBf128x2; }
 __device__ __forceinline__ uint32_t nib_lo_f16(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
 __device__ __forceinline__ uint32_t nib_hi_f16(uint32_t w) { return (w & 0x00F000F0u) | 0x54005400u; }
@@ -346,9 +353,9 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
 
   // online-softmax state of heads 2c (L) and 2c+1 (H); the same on the 8 lanes of a column
   float m_refL = -INFINITY, m_refH = -INFINITY, lsumL = 0.f, lsumH = 0.f;
-  float2 baccL = make_float2(0.f, 0.f), baccH = make_float2(0.f, 0.f);  // sum_j p_j b_jG (this thread's keys)
+  float2 baccL = make_float2(0.f, 0.f), baccH = make_float2(0.f, 0.f);  // sum_j p_j (b_jG + 8 s_jG) (this thread's keys)
   float oacc[C::MT][4];  // O^T: dims (mt, r / r+8) x heads (2c, 2c+1)
-  float corr[NG][4];     // 128 * sum_j B[j][head], heads (2c, 2c+1)
+  float corr[NG][4];     // 136 * sum_j B[j][head], heads (2c, 2c+1)
 #pragma unroll
   for (int G = 0; G < NG; ++G) corr[G][0] = corr[G][1] = corr[G][2] = corr[G][3] = 0.f;
 #pragma unroll
@@ -468,6 +475,11 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
         baccL = ffma2(make_float2(pv[2], pv[2]), vbB, baccL);
         baccH = ffma2(make_float2(pv[3], pv[3]), vbB, baccH);
       }
+      // the centre of the codes, 8 p_j s_jG, from the unrounded weights (0
+      // for keys past kv_len)
+      const float2 eight = make_float2(8.f, 8.f);
+      baccL = ffma2(eight, make_float2(wA[0].x + wB[0].x, wA[NG - 1].x + wB[NG - 1].x), baccL);
+      baccH = ffma2(eight, make_float2(wA[0].y + wB[0].y, wA[NG - 1].y + wB[NG - 1].y), baccH);
     }
     // ---- O^T += V^T P^T.  Thread (r, c) reads, for keys kv[0..3], the
     // code bytes 32G + 4r .. +3 of every group G; M-tile 4G + m takes byte
@@ -487,7 +499,7 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
         mma_bf16(oacc[4 * G + m], nib_lo_bf16(x01), nib_lo_bf16(x01 >> 4), nib_lo_bf16(x23),
                  nib_lo_bf16(x23 >> 4), bp[G][0], bp[G][1]);
       }
-      mma_bf16(corr[G], kBf128x2, kBf128x2, kBf128x2, kBf128x2, bp[G][0], bp[G][1]);
+      mma_bf16(corr[G], kBf136x2, kBf136x2, kBf136x2, kBf136x2, bp[G][0], bp[G][1]);
     }
   };
 
