@@ -25,9 +25,10 @@ about 2^-8 / sqrt(3) times that of o_d itself.  Measured over the test and
 config sizes on a GB300 the largest err / max|ref_r| was 2^-7.3 (prefill)
 and 2^-7.55 (decode); REL = 2^-6 keeps a factor of 2.4 or more.  4-bit
 caches: the B operand p * scale of the P.V product is rounded the same way
-but multiplies codes of up to 15 * scale (against values of about a third of
-that), and short contexts average few rows; measured up to 2^-6.8 at 64
-keys, so REL = 2^-5 (factor 3.4).  fp32 caches round nothing to bf16: the
+but multiplies centred codes c - 8 (up to 8 * scale, against values of about
+a third of that), and short contexts average few rows; measured up to
+2^-7.6 at 64 keys and 2^-7.4 with keys ramped to 40x (one head's weight on a
+few keys), so REL = 2^-5 (factor 4 or more).  fp32 caches round nothing to bf16: the
 error comes from ex2.approx (relative 2^-22) and fp32 accumulation, measured
 below 2^-21; REL = 2^-16.  FLOOR covers rows whose reference is 0 (a request
 without keys), which the kernels write as exact zeros.
