@@ -84,10 +84,11 @@ def test_paged_decode_ramped_scores(rising):
 
 @pytest.mark.parametrize("splits", [0, 1], ids=["planned", "one_split"])
 @pytest.mark.parametrize("rising", [True, False], ids=["rising", "falling"])
-def test_q4_decode_ramped_scores(rising, splits):
+@pytest.mark.parametrize("D", [64, 128])
+def test_q4_decode_ramped_scores(D, rising, splits):
     """The ramp is applied to K before quantization, so the scales (and the
     scores) grow along the cache; the oracle attends over the same codes."""
-    B, Hq, Hkv, D, S = 2, 32, 8, 128, 2048
+    B, Hq, Hkv, S = 2, 32, 8, 2048
     lens = [2048, 999]
     _, k, v = ramped_qkv(B, Hq, Hkv, D, S, torch.bfloat16, layer=41, rising=rising)
     q = inputs.randn((B, Hq, 1, D), inputs.tensor_seed(41, 0), torch.bfloat16, DEV)
