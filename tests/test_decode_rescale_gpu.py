@@ -1,6 +1,7 @@
-"""Decode with scores that grow along the keys, against the fp64 oracle.
+"""Decode and prefill with scores that grow along the keys, against the fp64
+oracle.
 
-Every decode kernel keeps a lazy running maximum: the reference is raised,
+Every kernel keeps a lazy running maximum: the reference is raised,
 and the accumulated output rescaled, only when a tile's maximum exceeds it by
 more than a factor 2^8.  With N(0,1) inputs that almost never happens after
 the first tile, so the ordinary parity tests barely reach the rescale code.
@@ -10,9 +11,10 @@ keep rising through every split's share of the keys and the rescale runs many
 times (at 3000 keys, 7 heads of one KV head: 37 rises past 2^8 with one
 split, 125 with three), in the fp32 and bf16 kernels, the paged kernel, the
 4-bit kernel (the ramp applied before quantization) and the stacked-layers
-launch.  A falling ramp (40 down to 1) checks the opposite extreme: the first
-tile holds the maximum and later probabilities underflow towards zero.  Split
-counts are forced too, including one split (the whole sequence in one CTA).
+launch, and the prefill kernel's work units.  A falling ramp (40 down to 1)
+checks the opposite extreme: the first tile holds the maximum and later
+probabilities underflow towards zero.  Split counts are forced too, including
+one split (the whole sequence in one CTA).
 Bounds of tests/parity.py.
 """
 
@@ -118,3 +120,26 @@ def test_stacked_layers_ramped_scores():
     for l in range(NL):
         ref = oracle.attention(f64(q[l]), f64(k[l]), f64(v[l]), scale=D ** -0.5)["o"]
         parity.check(f64(o[l]), ref, "f32", f"layer {l}")
+
+
+@pytest.mark.parametrize("unit", ["planned", "pairs", "single_tiles", "kv_split_2", "kv_split_4"])
+@pytest.mark.parametrize("rising", [True, False], ids=["rising", "falling"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("q_len,kv_len", [(1000, 1000), (300, 2000)], ids=["square", "chunk"])
+def test_prefill_ramped_scores(q_len, kv_len, D, rising, unit):
+    """Prefill under the same ramp (1 to 40 along the keys, or 40 to 1): the
+    lazy reference of every work-unit kind (pairs, single tiles whose odd
+    slot starts with no visible key, KV shares merged across a cluster)."""
+    Hq, Hkv = 14, 2
+    q = inputs.randn((1, Hq, q_len, D), inputs.tensor_seed(61, 0), torch.float32, DEV)
+    _, k, v = inputs.qkv(1, Hq, Hkv, D, 1, kv_len, torch.float32, layer=61, device=DEV)
+    k = k * ramp(kv_len, rising)
+    q, k, v = q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+    override = {"planned": {}, "pairs": {"prefill_interleave_from": 1 << 20},
+                "single_tiles": {"prefill_interleave_from": 0}, "kv_split_2": {"prefill_kv_split": 2},
+                "kv_split_4": {"prefill_kv_split": 4}}[unit]
+    with binding.plan_override(**override):
+        o = binding.prefill(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    ref = oracle.attention(f64(q), f64(k), f64(v), scale=D ** -0.5, causal=True)["o"]
+    parity.check(f64(o), ref, "bf16")
