@@ -1,7 +1,7 @@
 """Seeded random shapes against the oracle: prefill (D = 64 and 128, causal
 and full, chunks at an offset, every work-unit kind the planner can pick or
-the override forces) and decode (fp32 and bf16, ragged lengths with empty
-requests).  Bounds of tests/parity.py.  The shapes are drawn once from a fixed
+the override forces), decode (fp32 and bf16, ragged lengths with empty
+requests) and 4-bit decode.  Bounds of tests/parity.py.  The shapes are drawn once from a fixed
 seed, so a failure names a reproducible case.
 """
 
@@ -99,3 +99,42 @@ def test_decode_random_shape(i, B, Hq, Hkv, D, s_cap, dtype, lens):
         ref = oracle.attention(f64(q[b:b + 1]), f64(k[b:b + 1, :, :L]), f64(v[b:b + 1, :, :L]),
                                scale=D ** -0.5)["o"]
         parity.check(got[b:b + 1], ref, dtype, f"case {i} request {b}")
+
+
+def _q4_cases(n=16, seed=20261204):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        D = int(rng.choice([64, 128]))
+        Hq, Hkv = _heads(rng)
+        B = int(rng.integers(1, 5))
+        s_cap = 8 * int(rng.integers(1, 500))  # the 4-bit cache holds a multiple of 8 rows
+        lens = [int(x) for x in rng.integers(0, s_cap + 1, size=B)]
+        if rng.random() < 0.3:
+            lens = None
+        cases.append((i, B, Hq, Hkv, D, s_cap, lens))
+    return cases
+
+
+@pytest.mark.parametrize("i,B,Hq,Hkv,D,s_cap,lens", _q4_cases())
+def test_q4_decode_random_shape(i, B, Hq, Hkv, D, s_cap, lens):
+    """4-bit decode on random shapes; scales and biases past each request's
+    length are NaN, and a request without keys returns zeros."""
+    kc, ks, kb, vc, vs, vb = inputs.q4_cache(B, Hkv, D, s_cap, layer=300 + i, device=DEV)
+    q = inputs.randn((B, Hq, 1, D), inputs.tensor_seed(300 + i, 0), torch.bfloat16, DEV)
+    kv_lens = None
+    if lens is not None:
+        for t in (ks, kb, vs, vb):
+            inputs.poison_tail(t, lens)
+        kv_lens = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    o = binding.decode_q4(q, kc, ks, kb, vc, vs, vb, kv_lens=kv_lens)
+    torch.cuda.synchronize()
+    got = o.float().cpu().numpy()
+    ref = oracle.attention_q4(q.float().cpu().numpy(), kc.cpu().numpy(), ks.cpu().numpy(), kb.cpu().numpy(),
+                              vc.cpu().numpy(), vs.cpu().numpy(), vb.cpu().numpy(),
+                              kv_lens=lens, scale=D ** -0.5)["o"]
+    for b in range(B):
+        if lens is not None and lens[b] == 0:
+            assert (got[b] == 0).all(), f"case {i}: request {b} has no keys"
+            continue
+        parity.check(got[b:b + 1], ref[b:b + 1], "q4", f"case {i} request {b}")
