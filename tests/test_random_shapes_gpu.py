@@ -1,7 +1,7 @@
 """Seeded random shapes against the oracle: prefill (D = 64 and 128, causal
 and full, chunks at an offset, every work-unit kind the planner can pick or
-the override forces), decode (fp32 and bf16, ragged lengths with empty
-requests) and 4-bit decode.  Bounds of tests/parity.py.  The shapes are drawn once from a fixed
+the override forces, and per-request lengths), decode (fp32 and bf16, ragged
+lengths with empty requests) and 4-bit decode.  Bounds of tests/parity.py.  The shapes are drawn once from a fixed
 seed, so a failure names a reproducible case.
 """
 
@@ -138,3 +138,43 @@ def test_q4_decode_random_shape(i, B, Hq, Hkv, D, s_cap, lens):
             assert (got[b] == 0).all(), f"case {i}: request {b} has no keys"
             continue
         parity.check(got[b:b + 1], ref[b:b + 1], "q4", f"case {i} request {b}")
+
+
+def _varlen_cases(n=12, seed=20261205):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        D = int(rng.choice([64, 128]))
+        Hq, Hkv = _heads(rng)
+        B = int(rng.integers(1, 7))
+        kv = [int(x) for x in rng.integers(0, 1200, size=B)]
+        ql = [int(rng.integers(0, k + 1)) if rng.random() < 0.7 else k for k in kv]
+        causal = bool(rng.random() < 0.75)
+        cases.append((i, Hq, Hkv, D, ql, kv, causal))
+    return cases
+
+
+@pytest.mark.parametrize("i,Hq,Hkv,D,q_lens,kv_lens,causal", _varlen_cases())
+def test_prefill_varlen_random_shape(i, Hq, Hkv, D, q_lens, kv_lens, causal):
+    """Per-request query and key lengths (empty requests included), NaN past
+    each request's rows; rows past a request's queries keep their sentinel."""
+    B = len(q_lens)
+    Tq_cap, S_cap = max(max(q_lens), 1), max(max(kv_lens), 1)
+    q = inputs.randn((B, Hq, Tq_cap, D), inputs.tensor_seed(400 + i, 0), torch.bfloat16, DEV)
+    k = inputs.randn((B, Hkv, S_cap, D), inputs.tensor_seed(400 + i, 1), torch.bfloat16, DEV)
+    v = inputs.randn((B, Hkv, S_cap, D), inputs.tensor_seed(400 + i, 2), torch.bfloat16, DEV)
+    inputs.poison_tail(q, q_lens)
+    inputs.poison_tail(k, kv_lens)
+    inputs.poison_tail(v, kv_lens)
+    o = torch.full_like(q, 3.0)
+    binding.gqa_attn_prefill_varlen(q, k, v, o, torch.tensor(q_lens, dtype=torch.int32, device=DEV),
+                                    torch.tensor(kv_lens, dtype=torch.int32, device=DEV), D ** -0.5, causal=causal)
+    torch.cuda.synchronize()
+    got = f64(o)
+    for b, (qn, kn) in enumerate(zip(q_lens, kv_lens)):
+        assert (got[b, :, qn:] == 3.0).all(), f"case {i} request {b}: rows past q_len were written"
+        if qn == 0:
+            continue
+        ref = oracle.attention(f64(q[b:b + 1, :, :qn]), f64(k[b:b + 1, :, :kn]), f64(v[b:b + 1, :, :kn]),
+                               scale=D ** -0.5, causal=causal)["o"]
+        parity.check(got[b:b + 1, :, :qn], ref, "bf16", f"case {i} request {b}")
