@@ -104,3 +104,22 @@ def test_config_qwen3_4b_q4_36_layers(S):
             torch.cuda.synchronize()
             ref = oracle_o(q, cache, [S] * 4, 128)
             parity.check(o.float().cpu().numpy(), ref, "q4", f"layer {l}")
+
+
+@pytest.mark.parametrize("mag", [1e-3, 1e4, 1e6], ids=["small", "1e4", "1e6"])
+def test_q4_query_range(mag):
+    """q enters the score product as fp16, so a q with elements of 2^14 or
+    more is scaled by 2^-e inside the kernel and the scores by 2^e after.
+    Here q is multiplied by mag and the softmax scale divided by it, so the
+    scores keep their usual size while q spans fp16's range and beyond (e = 2
+    and 6 for 1e4 and 1e6; a small q takes no scaling)."""
+    B, Hq, Hkv, D, S = 2, 32, 8, 128, 1000
+    q, cache = make_case(B, Hq, Hkv, D, S, layer=71)
+    q = (q.float() * mag).to(torch.bfloat16)
+    lens_t = torch.tensor([S, 377], dtype=torch.int32, device=DEV)
+    o = binding.decode_q4(q, *cache, kv_lens=lens_t, scale=D ** -0.5 / mag)
+    torch.cuda.synchronize()
+    kc, ks, kb, vc, vs, vb = (t.cpu().numpy() for t in cache)
+    ref = oracle.attention_q4(q.float().cpu().numpy(), kc, ks, kb, vc, vs, vb, kv_lens=[S, 377],
+                              scale=D ** -0.5 / mag)["o"]
+    parity.check(o.float().cpu().numpy(), ref, "q4")
