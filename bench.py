@@ -1037,12 +1037,25 @@ def main():
               for q, k, v in host)
     d2h = sum(o.numel() * o.element_size() for o in host_out)
 
+    # Each layer's inputs are copied on a stream of their own and its call
+    # waits for them, so layer l attends while layer l + 1 is still copying;
+    # a step's copies wait for the previous step to be done with the buffers.
+    copy_stream = torch.cuda.Stream(device)
+
     def e2e_step():
-        for (hq, hk, hv), (q, k, v) in zip(host, layers):
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-        time_decode_step(binding, layers, outs, ws, S, stream)
+        copy_stream.wait_stream(stream)
+        landed = []
+        with torch.cuda.stream(copy_stream):
+            for (hq, hk, hv), (q, k, v) in zip(host, layers):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                landed.append(ev)
+        for ev, (q, k, v), o in zip(landed, layers, outs):
+            stream.wait_event(ev)
+            binding.gqa_attn_decode(q, k, v, o, None, D ** -0.5, ws, max_kv_len=S, stream=stream)
         for o, ho in zip(outs, host_out):
             ho.copy_(o, non_blocking=True)
 
