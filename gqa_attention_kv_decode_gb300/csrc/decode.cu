@@ -53,6 +53,7 @@ struct DecodeParams {
   float2* ml;     // [B][Hq][n_split] (max in log2 units, sum)
   float* part_o;  // [B][Hq][n_split][D] unnormalised partial outputs
   uint64_t wait_limit_ns;
+  uint64_t test_stall_ns;  // 0, or (tests) a wait that nothing ends, see the kernel
   // paged cache (PAGED kernels): k and v are pools [num_blocks][Hkv][block_size][D]
   const int32_t* block_table;  // [B][max_blocks]
   int block_size, max_blocks, num_blocks;
@@ -91,7 +92,7 @@ struct Cfg {
   static constexpr int OFF_Q = NSTAGE * STAGEB;
   static constexpr int OFF_P = OFF_Q + NREP_P * D * 4;
   static constexpr int OFF_BAR = OFF_P + NCW * TW * NREP_P * 8;
-  static constexpr int OFF_FLAG = OFF_BAR + NSTAGE * 8 + NSTAGE * 4;
+  static constexpr int OFF_FLAG = OFF_BAR + (NSTAGE + 1) * 8 + NSTAGE * 4;  // full[NSTAGE + 1], rel[NSTAGE]
   static constexpr int SMEM = OFF_FLAG + 16;
   static constexpr int MERGE_FLOATS = NCW * (NREP_P * D + 2 * NREP_P);
   static_assert(NCH % DS == 0, "row must split into 8 lanes of 16-byte chunks");
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
   float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
   float2* p_s = reinterpret_cast<float2*>(smem + C::OFF_P);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // copy landed
-  int* rel = reinterpret_cast<int*>(smem + C::OFF_BAR + NSTAGE * 8);  // warps done with a stage
+  int* rel = reinterpret_cast<int*>(smem + C::OFF_BAR + (NSTAGE + 1) * 8);  // warps done with a stage
   volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort [2] issued
 
   // Byte offset of key row `row` of this (request, KV head) in K or V.  For a
@@ -225,6 +226,15 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
     const uint64_t pol = l2_policy_evict_first();
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t, pol);
     flag[2] = min(NSTAGE, nt);
+    if (p.test_stall_ns != 0) {
+      // Test only (gqa_attn_set_decode_wait_test): wait, with the test's
+      // limit, on a barrier that nothing arrives on, as on a copy that never
+      // lands, and give up as such a wait does.  Every CTA then takes the
+      // path of a lost copy: no partials, the status bit, its copies drained
+      // (with the ordinary limit) before it returns.
+      mbar_init(&full[NSTAGE], 1);
+      if (!mbar_wait_bounded(&full[NSTAGE], 0u, p.test_stall_ns)) flag[0] = 1;
+    }
   }
   // q rows of this CTA's heads (contiguous in memory), pre-scaled, laid out so
   // that the 8 lanes of a row group read 8 consecutive 16-byte pieces:
@@ -617,6 +627,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
+  p.test_stall_ns = decode_wait_test_ns();
   p.block_table = a.block_table;
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;

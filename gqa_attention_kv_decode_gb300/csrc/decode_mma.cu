@@ -49,6 +49,7 @@ struct MmaParams {
   float2* ml;
   float* part_o;
   uint64_t wait_limit_ns;
+  uint64_t test_stall_ns;  // 0, or (tests) a wait that nothing ends, see the kernel
   // paged cache (PAGED kernels): the tensor maps span the pools
   // [num_blocks * Hkv][block_size][D]
   const int32_t* block_table;  // [B][max_blocks]
@@ -91,7 +92,7 @@ struct MmaCfg {
   static constexpr int TILEB = HALVES * BOX;  // K (or V) tile
   static constexpr int STAGEB = 2 * TILEB;    // K + V
   static constexpr int OFF_BAR = NSTAGE * STAGEB;
-  static constexpr int OFF_REL = OFF_BAR + NSTAGE * 8;
+  static constexpr int OFF_REL = OFF_BAR + (NSTAGE + 1) * 8;  // after full[NSTAGE + 1]
   static constexpr int OFF_FLAG = OFF_REL + NSTAGE * 4;
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + slack for the 1024-byte alignment of the boxes
   static constexpr int KSTEPS = D / 16;       // k-steps of S = Q K^T
@@ -270,6 +271,15 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
     flag[1] = 0;
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t);
     flag[2] = min(NSTAGE, nt);
+    if (p.test_stall_ns != 0) {
+      // Test only (gqa_attn_set_decode_wait_test): wait, with the test's
+      // limit, on a barrier that nothing arrives on, as on a copy that never
+      // lands, and give up as such a wait does.  Every CTA then takes the
+      // path of a lost copy: no partials, the status bit, its copies drained
+      // (with the ordinary limit) before it returns.
+      mbar_init(&full[NSTAGE], 1);
+      if (!mbar_wait_bounded(&full[NSTAGE], 0u, p.test_stall_ns)) flag[0] = 1;
+    }
   }
   // Q as A fragments: row = query head lane/4 (zero past nh), k = dims.
   const int r = lane >> 2, c = lane & 3;
@@ -547,6 +557,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
+  p.test_stall_ns = decode_wait_test_ns();
   p.block_table = a.block_table;
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;

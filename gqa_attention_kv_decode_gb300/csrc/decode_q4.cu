@@ -71,6 +71,7 @@ struct Q4Params {
   float2* ml;
   float* part_o;
   uint64_t wait_limit_ns;
+  uint64_t test_stall_ns;  // 0, or (tests) a wait that nothing ends, see the kernel
   int n_slots;        // partial slots per (request, head) row in the workspace
   int force_partial;  // write partials even for a one-split request (a residual window follows)
 };
@@ -97,7 +98,7 @@ struct Q4Cfg {
   static constexpr int OFF_SC = NSTAGE * STAGEB;
   static constexpr int OFF_QA = OFF_SC + NW * SCW * 4;   // q fragments: [KSTEPS/2][lane][4] words
   static constexpr int OFF_BAR = OFF_QA + KSTEPS / 2 * 32 * 16;
-  static constexpr int OFF_REL = OFF_BAR + NSTAGE * 8;
+  static constexpr int OFF_REL = OFF_BAR + (NSTAGE + 1) * 8;  // after full[NSTAGE + 1]
   static constexpr int OFF_FLAG = OFF_REL + ((NSTAGE * 4 + 15) / 16) * 16;
   static constexpr int SMEM = OFF_FLAG + 16;
   static constexpr int MERGE_FLOATS = NW * (8 * D + 16);  // per warp: O[8][D], m[8], l[8]
@@ -253,6 +254,15 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
     flag[1] = 0;
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t, pol);
     flag[2] = min(NSTAGE, nt);
+    if (p.test_stall_ns != 0) {
+      // Test only (gqa_attn_set_decode_wait_test): wait, with the test's
+      // limit, on a barrier that nothing arrives on, as on a copy that never
+      // lands, and give up as such a wait does.  Every CTA then takes the
+      // path of a lost copy: no partials, the status bit, its copies drained
+      // (with the ordinary limit) before it returns.
+      mbar_init(&full[NSTAGE], 1);
+      if (!mbar_wait_bounded(&full[NSTAGE], 0u, p.test_stall_ns)) flag[0] = 1;
+    }
   }
 
   // ---- q of head r as fp16 B fragments of S^T = K Q^T.  Thread (r, c)
@@ -676,6 +686,7 @@ cudaError_t launch_decode_q4(const DecodeQ4Args& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
+  p.test_stall_ns = decode_wait_test_ns();
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   cudaError_t e = a.D == 128 ? launch_q4_mma<128, kQ4Stages128>(p, grid, stream)
                              : launch_q4_mma<64, kQ4Stages64>(p, grid, stream);
