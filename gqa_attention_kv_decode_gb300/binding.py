@@ -56,7 +56,7 @@ EXPORTED = (
     "gqa_attn_version",
     "gqa_attn_set_plan_override",
     "gqa_attn_set_prefill_interleave_override",
-    "gqa_attn_set_decode_wait_test",
+    "gqa_attn_set_wait_test",
     "gqa_attn_read_prefill_status",
     "gqa_attn_clear_prefill_status",
 )
@@ -127,8 +127,8 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_set_plan_override.restype = i32
     L.gqa_attn_set_prefill_interleave_override.argtypes = [i32]
     L.gqa_attn_set_prefill_interleave_override.restype = i32
-    L.gqa_attn_set_decode_wait_test.argtypes = [ctypes.c_uint64]
-    L.gqa_attn_set_decode_wait_test.restype = i32
+    L.gqa_attn_set_wait_test.argtypes = [ctypes.c_uint64]
+    L.gqa_attn_set_wait_test.restype = i32
     L.gqa_attn_read_prefill_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
     L.gqa_attn_read_prefill_status.restype = i32
     L.gqa_attn_clear_prefill_status.argtypes = [vp]
@@ -183,11 +183,11 @@ def gqa_attn_set_plan_override(decode_splits=0, prefill_kv_split=0) -> None:
            "gqa_attn_set_plan_override")
 
 
-def gqa_attn_set_decode_wait_test(stall_ns=0) -> None:
-    """Tests only: later decode launches take the path of a tile copy that
-    never lands (a wait of stall_ns on a barrier nothing arrives on), so they
-    report GQA_DEV_WAIT_TIMEOUT; 0 turns it off."""
-    _check(lib().gqa_attn_set_decode_wait_test(int(stall_ns)), "gqa_attn_set_decode_wait_test")
+def gqa_attn_set_wait_test(stall_ns=0) -> None:
+    """Tests only: later decode and prefill launches take the path of a copy
+    that never lands (a wait of stall_ns on a barrier nothing arrives on), so
+    they report GQA_DEV_WAIT_TIMEOUT; 0 turns it off."""
+    _check(lib().gqa_attn_set_wait_test(int(stall_ns)), "gqa_attn_set_wait_test")
 
 
 def gqa_attn_set_prefill_interleave_override(from_pair=-1) -> None:

@@ -33,9 +33,9 @@ static std::atomic<int> g_prefill_kv_split_override{0};
 int prefill_kv_split_override() { return g_prefill_kv_split_override.load(std::memory_order_relaxed); }
 static std::atomic<int> g_prefill_interleave_override{-1};
 int prefill_interleave_override() { return g_prefill_interleave_override.load(std::memory_order_relaxed); }
-// Decode wait test (gqa_attn_set_decode_wait_test); 0 = off.
-static std::atomic<uint64_t> g_decode_wait_test_ns{0};
-uint64_t decode_wait_test_ns() { return g_decode_wait_test_ns.load(std::memory_order_relaxed); }
+// Failure-path test (gqa_attn_set_wait_test); 0 = off.
+static std::atomic<uint64_t> g_wait_test_ns{0};
+uint64_t wait_test_ns() { return g_wait_test_ns.load(std::memory_order_relaxed); }
 
 // Chooses how many key splits each (request, KV head) gets so that the grid
 // covers at most ctas_per_sm CTAs per SM (one wave) when requests are few and
@@ -162,9 +162,9 @@ GQA_ATTN_API int gqa_attn_set_prefill_interleave_override(int from_pair) {
   return GQA_OK;
 }
 
-GQA_ATTN_API int gqa_attn_set_decode_wait_test(uint64_t stall_ns) {
+GQA_ATTN_API int gqa_attn_set_wait_test(uint64_t stall_ns) {
   if (stall_ns > kWaitLimitNs) return GQA_ERR_INVALID_ARG;
-  g_decode_wait_test_ns.store(stall_ns, std::memory_order_relaxed);
+  g_wait_test_ns.store(stall_ns, std::memory_order_relaxed);
   return GQA_OK;
 }
 

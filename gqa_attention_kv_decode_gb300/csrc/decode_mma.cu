@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t);
     flag[2] = min(NSTAGE, nt);
     if (p.test_stall_ns != 0) {
-      // Test only (gqa_attn_set_decode_wait_test): wait, with the test's
+      // Test only (gqa_attn_set_wait_test): wait, with the test's
       // limit, on a barrier that nothing arrives on, as on a copy that never
       // lands, and give up as such a wait does.  Every CTA then takes the
       // path of a lost copy: no partials, the status bit, its copies drained
@@ -557,7 +557,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
-  p.test_stall_ns = decode_wait_test_ns();
+  p.test_stall_ns = wait_test_ns();
   p.block_table = a.block_table;
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;

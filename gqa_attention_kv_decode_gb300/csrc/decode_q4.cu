@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
     for (int t = 0; t < NSTAGE && t < nt; ++t) issue(t, t, pol);
     flag[2] = min(NSTAGE, nt);
     if (p.test_stall_ns != 0) {
-      // Test only (gqa_attn_set_decode_wait_test): wait, with the test's
+      // Test only (gqa_attn_set_wait_test): wait, with the test's
       // limit, on a barrier that nothing arrives on, as on a copy that never
       // lands, and give up as such a wait does.  Every CTA then takes the
       // path of a lost copy: no partials, the status bit, its copies drained
@@ -686,7 +686,7 @@ cudaError_t launch_decode_q4(const DecodeQ4Args& a, cudaStream_t stream) {
   p.ml = reinterpret_cast<float2*>(ws + w.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + w.off_o);
   p.wait_limit_ns = kWaitLimitNs;
-  p.test_stall_ns = decode_wait_test_ns();
+  p.test_stall_ns = wait_test_ns();
   const dim3 grid(a.plan.n_split, a.Hkv * a.plan.n_hc, a.B);
   cudaError_t e = a.D == 128 ? launch_q4_mma<128, kQ4Stages128>(p, grid, stream)
                              : launch_q4_mma<64, kQ4Stages64>(p, grid, stream);

@@ -50,7 +50,7 @@ int device_sm_count();
 int prefill_kv_split_override();
 // Forced first interleaved pair of prefill (>= 0), or -1 for the planner's choice.
 int prefill_interleave_override();
-uint64_t decode_wait_test_ns();  // gqa_attn_set_decode_wait_test; 0 = off
+uint64_t wait_test_ns();  // gqa_attn_set_wait_test; 0 = off
 
 // Shape, dtype and pointer checks shared by gqa_attn_decode and
 // gqa_attn_decode_noalloc (everything but the workspace); GQA_OK or an error.

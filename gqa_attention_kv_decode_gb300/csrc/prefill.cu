@@ -96,10 +96,12 @@ struct PfCfg {
   //   B_P0[t]  P_t keys 0..63 stored            B_P1[t]  P_t keys 64..127 stored
   //   B_O0[t]  P.V over keys 0..63 done         B_O1[t]  P.V over all keys done
   //   B_DRAIN  after a timed-out wait: the MMA-issuing warps' work is done
+  //   B_STALL  nothing arrives on it (the failure-path test waits on it)
   static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_S = B_KE + NST,
                        B_SC = B_S + 2, B_P0 = B_SC + 2, B_P1 = B_P0 + 2, B_O0 = B_P1 + 2, B_O1 = B_O0 + 2,
-                       B_DRAIN = B_O1 + 2, N_BARS = B_DRAIN + 1;
-  static constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8, OFF_UNIT = OFF_ABORT + 4;
+                       B_DRAIN = B_O1 + 2, B_STALL = B_DRAIN + 1, N_BARS = B_STALL + 1;
+  static constexpr int OFF_TSLOT = 8 * N_BARS, OFF_ABORT = OFF_TSLOT + 8, OFF_UNIT = OFF_ABORT + 4,
+                       OFF_ISSUED = OFF_UNIT + 8;
   // Split-KV exchange (after the main loop, over Q and the K/V stages): a
   // partial row is (O[HD], m, l) padded to HD/4 + 1 float4 chunks; a unit is
   // 32 rows of one tile, stored chunk-major ([chunk][row][4]) so that the 32
@@ -109,7 +111,7 @@ struct PfCfg {
   static constexpr int XCHUNKS = HD / 4 + 1, XUNIT = XCHUNKS * 32 * 4;  // floats per unit
   static constexpr int X_MAX_UNITS = OFF_BAR / (XUNIT * 4);
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-  static_assert(OFF_UNIT + 8 <= 256, "barrier area");
+  static_assert(OFF_ISSUED + 4 <= 256, "barrier area");
   static_assert(HD == 64 || HD == 128, "head dimension");
   static_assert(128 * REG_CTRL + 256 * REG_SOFTMAX <= NTHR * 168, "register split exceeds the launch allocation");
 };
@@ -142,6 +144,7 @@ struct PrefillParams {
   int kv_splits;        // CTAs of a cluster sharing one pair's KV tiles (1 to 8)
   float qk_scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  uint64_t test_stall_ns;  // 0, or (tests) a wait that nothing ends, see the TMA role
   int q_pitch;          // rows per head of Q and O
   // per-request lengths (varlen; null: q_len, kv_len for every request):
   // request b has clamp(kv_lens[b], 0, kv_len) keys and clamp(q_lens[b], 0,
@@ -340,12 +343,15 @@ __global__ void __launch_bounds__(NTHR, 1)
   const uint32_t tmem = *tslot;
   if (p.q_lens == nullptr) grid_dependency_wait();
 
+  // K/V tiles the TMA thread has copied, for the drain after a timed-out wait
+  volatile int* n_issued_s = reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_ISSUED);
   if (warp >= 8) {
     set_max_regs_dec<C::REG_CTRL>();
     if (warp == 8 && lane == 0) {
       // ---------------- TMA ----------------
       const int kv_head = b * p.Hkv + g;
       const int n_q = ilv ? 1 : 2;  // a single-tile unit reads Q_A only
+      int n_issued = 0;
       mbar_arrive_expect_tx(&bars[B_Q], n_q * TILE_BYTES);
       for (int t = 0; t < n_q; ++t)
 #pragma unroll
@@ -366,7 +372,15 @@ __global__ void __launch_bounds__(NTHR, 1)
         for (int bx = 0; bx < NBOX; ++bx)
           tma_load_3d(smem + OFF_V + st * TILE_BYTES + bx * BOX_BYTES, &tmV, bx * 64, (j_lo + j) * BN, kv_head,
                       &bars[B_VF + st]);
+        n_issued = j + 1;
+        if (p.test_stall_ns != 0 && n_issued == min(NST, nkv_max)) {
+          // Test only (gqa_attn_set_wait_test): wait, with the test's limit,
+          // on a barrier that nothing arrives on, as on a stage that is never
+          // released, and give up as such a wait does.
+          if (!mbar_wait_bounded(&bars[C::B_STALL], 0u, p.test_stall_ns)) *abort_flag = 1;
+        }
       }
+      *n_issued_s = n_issued;
     } else if (warp == 9) {
       // ---------------- MMA issue: S_t = Q_t K^T ----------------
       // Three warps issue tcgen05.mma (this one the scores, warps 10 and 11
@@ -757,6 +771,17 @@ __global__ void __launch_bounds__(NTHR, 1)
       mma_commit_warp(&bars[B_DRAIN]);
       mbar_wait_bounded(&bars[B_DRAIN], 0, p.wait_limit_ns);
     }
+    if (warp == 8 && lane == 0) {
+      // and the copies in flight land before the shared memory is released:
+      // Q, and the last tile copied into each stage
+      mbar_wait_bounded(&bars[B_Q], 0u, p.wait_limit_ns);
+      const int n_issued = *n_issued_s;
+      for (int s = 0; s < NST && s < n_issued; ++s) {
+        const int u = s + ((n_issued - 1 - s) / NST) * NST;
+        mbar_wait_bounded(&bars[B_KF + s], uint32_t(u / NST) & 1u, p.wait_limit_ns);
+        mbar_wait_bounded(&bars[B_VF + s], uint32_t(u / NST) & 1u, p.wait_limit_ns);
+      }
+    }
     if (tid == 0) atomicOr(&g_prefill_status, GQA_DEV_WAIT_TIMEOUT);
     tc_fence_before();
     __syncthreads();
@@ -891,6 +916,7 @@ cudaError_t launch_prefill_hd(const PrefillArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.qk_scale_log2 = float(double(a.scale) * 1.4426950408889634);
   p.wait_limit_ns = kWaitLimitNs;
+  p.test_stall_ns = wait_test_ns();
   // Split the KV range of a pair over a cluster when the pairs alone leave
   // SMs idle: as many CTAs per pair (up to 8) as keep the grid within one
   // wave and every share at kMinShareTiles KV tiles or more.  (Beyond one

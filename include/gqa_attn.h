@@ -303,19 +303,22 @@ GQA_ATTN_API int gqa_attn_set_plan_override(int decode_splits, int prefill_kv_sp
  * Returns GQA_OK. */
 GQA_ATTN_API int gqa_attn_set_prefill_interleave_override(int from_pair);
 
-/* Failure-path test of the decode kernels, for tests only.  Every wait of a
- * decode kernel on a tile copy gives up after 1 s; the CTA then lets the
- * copies it issued land (waiting with the same 1 s limit), writes no
- * partials, sets GQA_DEV_WAIT_TIMEOUT in the workspace status word and
- * returns, leaving the context usable.  With stall_ns > 0 every later launch
- * of gqa_attn_decode, _decode_paged, _decode_layers, _decode_q4 and
- * _decode_q4_residual makes the first thread of each CTA, after it has issued
- * its first copies, wait stall_ns on a barrier that nothing arrives on, so
- * that this path runs deterministically: the call sets GQA_DEV_WAIT_TIMEOUT
- * and its outputs are unspecified.  0 (the initial setting) turns it off.
- * stall_ns > 10^9 returns GQA_ERR_INVALID_ARG; otherwise GQA_OK.  Same
- * threading rules as gqa_attn_set_plan_override. */
-GQA_ATTN_API int gqa_attn_set_decode_wait_test(uint64_t stall_ns);
+/* Failure-path test of the kernels, for tests only.  Every wait of a kernel
+ * on a copy or a product gives up after 1 s; the CTA then lets the copies it
+ * issued land (waiting with the same 1 s limit) and returns, leaving the
+ * context usable: a decode CTA writes no partials and sets
+ * GQA_DEV_WAIT_TIMEOUT in the workspace status word, a prefill CTA writes its
+ * output rows as NaN and sets GQA_DEV_WAIT_TIMEOUT in the prefill status word.
+ * With stall_ns > 0 every later launch of gqa_attn_decode, _decode_paged,
+ * _decode_layers, _decode_q4, _decode_q4_residual, _prefill and
+ * _prefill_varlen makes the thread that issues a CTA's copies, once it has
+ * issued its first ones, wait stall_ns on a barrier that nothing arrives on
+ * and give up, so that this path runs deterministically: the call reports
+ * GQA_DEV_WAIT_TIMEOUT and its outputs are unspecified (a prefill CTA whose
+ * copies were all issued before the stall may finish its rows normally).
+ * 0 (the initial setting) turns it off.  stall_ns > 10^9 returns GQA_ERR_INVALID_ARG;
+ * otherwise GQA_OK.  Same threading rules as gqa_attn_set_plan_override. */
+GQA_ATTN_API int gqa_attn_set_wait_test(uint64_t stall_ns);
 
 /* ---------------------------------------------------------------------------
  * Single-token decode without any caller-provided or allocated scratch.

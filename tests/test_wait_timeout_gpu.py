@@ -1,15 +1,17 @@
-"""The decode kernels' lost-copy path, forced without faulting anything.
+"""The kernels' lost-copy path, forced without faulting anything.
 
-Every wait of a decode kernel on a tile copy gives up after a time limit; the
-CTA then drains the copies it issued, writes no partials, sets
-GQA_DEV_WAIT_TIMEOUT in the workspace status word and returns.  A real lost
-copy cannot be produced safely, so gqa_attn_set_decode_wait_test makes the
-first thread of every CTA wait, after issuing its first copies, on a barrier
-that nothing arrives on (a bounded wait of 100 us here), which sends every
-CTA down that path.  The test checks that the status word reports it, and
-that the same context then computes a correct result (the GPU stays usable),
-for the fp32 and bf16 kernels (both bf16 shapes), the paged, 4-bit and
-stacked-layers launches.
+Every wait of a kernel on a copy or a product gives up after a time limit;
+the CTA then drains what it issued and returns: a decode CTA writes no
+partials and sets GQA_DEV_WAIT_TIMEOUT in the workspace status word, a
+prefill CTA writes its rows as NaN and sets it in the prefill status word.
+A real lost copy cannot be produced safely, so gqa_attn_set_wait_test makes
+the thread that issues a CTA's copies wait, after its first ones, on a
+barrier that nothing arrives on (a bounded wait of 100 us here), which sends
+every CTA down that path.  The tests check that the status word reports it
+and that the same context then computes a correct result (the GPU stays
+usable): the fp32 and bf16 decode kernels (both bf16 shapes), the paged,
+4-bit and stacked-layers launches, and prefill at D = 64 and 128 in pairs,
+single-tile units, KV splits over clusters and with per-request lengths.
 """
 
 import contextlib
@@ -35,11 +37,11 @@ def _built():
 
 @contextlib.contextmanager
 def lost_copies():
-    binding.gqa_attn_set_decode_wait_test(STALL_NS)
+    binding.gqa_attn_set_wait_test(STALL_NS)
     try:
         yield
     finally:
-        binding.gqa_attn_set_decode_wait_test(0)
+        binding.gqa_attn_set_wait_test(0)
 
 
 def f64(t):
@@ -129,5 +131,52 @@ def test_stacked_layers_lost_copy_is_reported():
 
 def test_wait_test_rejects_limits_past_one_second():
     with pytest.raises(binding.GqaAttnError) as e:
-        binding.gqa_attn_set_decode_wait_test(2_000_000_000)
+        binding.gqa_attn_set_wait_test(2_000_000_000)
     assert e.value.status == binding.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case", ["pairs", "single_tiles", "kv_split", "varlen"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_lost_copy_is_reported_and_the_context_survives(D, case):
+    """Prefill's TMA thread stalls after its first copies: the CTA drains its
+    products and copies, writes the rows that waited on it as NaN and flags
+    the prefill status word; the next call on the same context is correct."""
+    Hq, Hkv = 14, 2
+    q_len, kv_len = (300, 2000) if case == "kv_split" else (1000, 1000)
+    q = inputs.randn((2 if case == "varlen" else 1, Hq, q_len, D), 111, torch.bfloat16, DEV)
+    k = inputs.randn((q.shape[0], Hkv, kv_len, D), 112, torch.bfloat16, DEV)
+    v = inputs.randn((q.shape[0], Hkv, kv_len, D), 113, torch.bfloat16, DEV)
+    override = {"pairs": {"prefill_interleave_from": 1 << 20}, "single_tiles": {"prefill_interleave_from": 0},
+                "kv_split": {"prefill_kv_split": 4}, "varlen": {}}[case]
+    lens = [1000, 700]
+
+    def run():
+        o = torch.full_like(q, 3.0)
+        with binding.plan_override(**override):
+            if case == "varlen":
+                binding.gqa_attn_prefill_varlen(q, k, v, o, torch.tensor(lens, dtype=torch.int32, device=DEV),
+                                                torch.tensor(lens, dtype=torch.int32, device=DEV), D ** -0.5)
+            else:
+                binding.gqa_attn_prefill(q, k, v, o, kv_len, D ** -0.5, True)
+        torch.cuda.synchronize()
+        return o
+
+    binding.gqa_attn_clear_prefill_status()
+    with lost_copies():
+        o = run()
+    assert binding.gqa_attn_read_prefill_status() & binding.GQA_DEV_WAIT_TIMEOUT
+    rows = lens if case == "varlen" else [q_len]
+    # The last query rows belong to the unit with the most KV tiles, more than
+    # the stages hold, so its work waited on copies that were never issued:
+    # those rows are NaN.  (A unit whose copies were all issued before the
+    # stall may finish normally.)
+    for b, n in enumerate(rows):
+        assert torch.isnan(o[b, :, n - 1].float()).all(), "rows that waited on a lost copy are NaN"
+    binding.gqa_attn_clear_prefill_status()
+    o = run()
+    assert not binding.gqa_attn_read_prefill_status() & binding.GQA_DEV_WAIT_TIMEOUT
+    for b, n in enumerate(rows):
+        kn = n if case == "varlen" else kv_len
+        ref = oracle.attention(f64(q[b:b + 1, :, :n]), f64(k[b:b + 1, :, :kn]), f64(v[b:b + 1, :, :kn]),
+                               scale=D ** -0.5, causal=True)["o"]
+        parity.check(f64(o[b:b + 1, :, :n]), ref, "bf16", f"request {b}")
