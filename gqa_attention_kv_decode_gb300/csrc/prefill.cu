@@ -221,6 +221,28 @@ __device__ __forceinline__ void exp_half(const uint32_t* s, float2 c, float2 mm,
   }
 }
 
+// After a timed-out wait: lets the copies still in flight land before the
+// shared memory is released -- Q, and the last of the n_issued K/V tiles in
+// each of the NST stages.  Out of line: it runs only on that path, and
+// inlined it cost the D = 128 kernel 2% in the hot loop.
+template <int NST>
+__device__ __noinline__ void drain_copies(uint64_t* bars, int b_q, int b_kf, int b_vf, int n_issued,
+                                          uint64_t limit_ns) {
+  mbar_wait_bounded(&bars[b_q], 0u, limit_ns);
+  for (int s = 0; s < NST && s < n_issued; ++s) {
+    const int u = s + ((n_issued - 1 - s) / NST) * NST;
+    mbar_wait_bounded(&bars[b_kf + s], uint32_t(u / NST) & 1u, limit_ns);
+    mbar_wait_bounded(&bars[b_vf + s], uint32_t(u / NST) & 1u, limit_ns);
+  }
+}
+
+// Test only (gqa_attn_set_wait_test): waits, with the test's limit, on a
+// barrier that nothing arrives on, as on a copy that never lands, and gives
+// up as such a wait does.  Out of line, like the drain.
+__device__ __noinline__ void stall_test(uint64_t* bar, uint64_t stall_ns, volatile int* abort_flag) {
+  if (!mbar_wait_bounded(bar, 0u, stall_ns)) *abort_flag = 1;
+}
+
 // HD: head dimension (64 or 128).  SPLIT: the pair's KV range is shared by a
 // cluster of p.kv_splits CTAs whose partial rows are merged through
 // distributed shared memory.  ILV: the grid also holds single-tile units (see
@@ -343,8 +365,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   const uint32_t tmem = *tslot;
   if (p.q_lens == nullptr) grid_dependency_wait();
 
-  // K/V tiles the TMA thread has copied, for the drain after a timed-out wait
-  volatile int* n_issued_s = reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_ISSUED);
   if (warp >= 8) {
     set_max_regs_dec<C::REG_CTRL>();
     if (warp == 8 && lane == 0) {
@@ -352,6 +372,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int kv_head = b * p.Hkv + g;
       const int n_q = ilv ? 1 : 2;  // a single-tile unit reads Q_A only
       int n_issued = 0;
+      // (test only: Q is in flight, no K/V tile yet)
+      if (p.test_stall_ns != 0) stall_test(&bars[C::B_STALL], p.test_stall_ns, abort_flag);
       mbar_arrive_expect_tx(&bars[B_Q], n_q * TILE_BYTES);
       for (int t = 0; t < n_q; ++t)
 #pragma unroll
@@ -373,14 +395,9 @@ __global__ void __launch_bounds__(NTHR, 1)
           tma_load_3d(smem + OFF_V + st * TILE_BYTES + bx * BOX_BYTES, &tmV, bx * 64, (j_lo + j) * BN, kv_head,
                       &bars[B_VF + st]);
         n_issued = j + 1;
-        if (p.test_stall_ns != 0 && n_issued == min(NST, nkv_max)) {
-          // Test only (gqa_attn_set_wait_test): wait, with the test's limit,
-          // on a barrier that nothing arrives on, as on a stage that is never
-          // released, and give up as such a wait does.
-          if (!mbar_wait_bounded(&bars[C::B_STALL], 0u, p.test_stall_ns)) *abort_flag = 1;
-        }
       }
-      *n_issued_s = n_issued;
+      // the K/V tiles copied, for the drain after a timed-out wait
+      *reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_ISSUED) = n_issued;
     } else if (warp == 9) {
       // ---------------- MMA issue: S_t = Q_t K^T ----------------
       // Three warps issue tcgen05.mma (this one the scores, warps 10 and 11
@@ -771,17 +788,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       mma_commit_warp(&bars[B_DRAIN]);
       mbar_wait_bounded(&bars[B_DRAIN], 0, p.wait_limit_ns);
     }
-    if (warp == 8 && lane == 0) {
-      // and the copies in flight land before the shared memory is released:
-      // Q, and the last tile copied into each stage
-      mbar_wait_bounded(&bars[B_Q], 0u, p.wait_limit_ns);
-      const int n_issued = *n_issued_s;
-      for (int s = 0; s < NST && s < n_issued; ++s) {
-        const int u = s + ((n_issued - 1 - s) / NST) * NST;
-        mbar_wait_bounded(&bars[B_KF + s], uint32_t(u / NST) & 1u, p.wait_limit_ns);
-        mbar_wait_bounded(&bars[B_VF + s], uint32_t(u / NST) & 1u, p.wait_limit_ns);
-      }
-    }
+    if (warp == 8 && lane == 0)  // and the copies in flight land before the shared memory is released
+      drain_copies<NST>(bars, B_Q, B_KF, B_VF, *reinterpret_cast<volatile int*>(smem + OFF_BAR + C::OFF_ISSUED),
+                        p.wait_limit_ns);
     if (tid == 0) atomicOr(&g_prefill_status, GQA_DEV_WAIT_TIMEOUT);
     tc_fence_before();
     __syncthreads();
