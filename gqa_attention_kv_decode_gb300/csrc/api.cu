@@ -13,15 +13,15 @@
 namespace gqa {
 
 int device_sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // 0 until queried (zero-initialised as a static)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 static long ceil_div(long a, long b) { return (a + b - 1) / b; }

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "gqa_attn.h"
 #include "internal.h"
@@ -551,16 +552,15 @@ template <typename T, int D, int NREP, int R, int NSTAGE, bool PAGED>
 cudaError_t launch_one(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   using C = Cfg<T, D, NREP, R, NSTAGE>;
   auto kern = decode_split_kernel<T, D, NREP, R, NSTAGE, PAGED>;
-  static bool configured = false;  // per instantiation; attribute is per-function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    // two CTAs per SM need the largest shared-memory carveout
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::once_flag once;  // per instantiation; the attributes are per function
+  static cudaError_t cfg_err = cudaSuccess;
+  std::call_once(once, [&] {
+    cfg_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cfg_err == cudaSuccess)  // the largest shared-memory carveout
+      cfg_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+  });
+  if (cfg_err != cudaSuccess) return cfg_err;
   return launch_pdl(kern, grid, dim3(C::NTHR), C::SMEM, stream, p);
 }
 

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "gqa_attn.h"
@@ -632,16 +633,15 @@ template <int D, int NSTAGE>
 cudaError_t launch_q4_mma(const Q4Params& p, dim3 grid, cudaStream_t stream) {
   using C = Q4Cfg<D, NSTAGE>;
   auto kern = decode_q4_mma_kernel<D, NSTAGE>;
-  static bool configured = false;  // per instantiation; attributes are per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    // four CTAs per SM need the largest shared-memory carveout
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::once_flag once;  // per instantiation; the attributes are per function
+  static cudaError_t cfg_err = cudaSuccess;
+  std::call_once(once, [&] {
+    cfg_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cfg_err == cudaSuccess)  // four CTAs per SM need the largest shared-memory carveout
+      cfg_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+  });
+  if (cfg_err != cudaSuccess) return cfg_err;
   return launch_pdl(kern, grid, dim3(C::NTHR), C::SMEM, stream, p);
 }
 

@@ -961,16 +961,16 @@ cudaError_t launch_prefill_hd(const PrefillArgs& a, cudaStream_t stream) {
     p.ilv_from = up.ilv_from;
     p.n_first = up.n_first;
   }
-  static bool configured = false;
-  if (!configured) {
+  static std::once_flag once;
+  static cudaError_t cfg_err = cudaSuccess;
+  std::call_once(once, [&] {
     for (const void* k : {reinterpret_cast<const void*>(prefill_kernel<HD, false, false>),
                           reinterpret_cast<const void*>(prefill_kernel<HD, true, false>),
-                          reinterpret_cast<const void*>(prefill_kernel<HD, false, true>)}) {
-      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-    }
-    configured = true;
-  }
+                          reinterpret_cast<const void*>(prefill_kernel<HD, false, true>)})
+      if (cfg_err == cudaSuccess)
+        cfg_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  });
+  if (cfg_err != cudaSuccess) return cfg_err;
   const dim3 grid(a.B * a.Hq * p.kv_splits, std::max(0, p.n_tiles - 2 * p.ilv_from) + p.ilv_from);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

@@ -38,9 +38,21 @@ inline bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t cols, 
   cuuint64_t strides[2] = {cols * 2, row_pitch * cols * 2};
   cuuint32_t box[3] = {box_cols, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  auto encode = [&] {
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
+  CUresult r = encode();
+  if (r == CUDA_ERROR_INVALID_CONTEXT) {
+    // The driver call needs a current context, and the runtime makes the
+    // device's primary context current only on its first call that needs
+    // one, which a thread whose first CUDA work is this call has not made
+    // yet: make it now, then encode again.
+    if (cudaFree(nullptr) != cudaSuccess) return false;
+    r = encode();
+  }
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace gqa
