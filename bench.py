@@ -1073,6 +1073,20 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
     e2e_value = replica_value(world, step_bytes, e2e_ms)
+    # the same step's host-to-device copies alone: the rate of the host link,
+    # which bounds the end-to-end number (the attention calls hide under it)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(copy_stream)
+    with torch.cuda.stream(copy_stream):
+        for _ in range(e2e_steps):
+            for (hq, hk, hv), (q, k, v) in zip(host, layers):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+    c1.record(copy_stream)
+    torch.cuda.synchronize()
+    copy_ms = dist.max(c0.elapsed_time(c1)) / e2e_steps
     del host, host_out
 
     traffic = recorded_traffic("decode.cu", "decode_f32_d128_nrep7_S32768")
@@ -1115,7 +1129,12 @@ def main():
                      "isolated_kernel_frac": isolated_kernel_frac,
                      "n_split": n_split},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "h2d_copies_alone": {"ms_per_step": round(copy_ms, 3),
+                                     "h2d_gbs": round(h2d / copy_ms / 1e6, 1),
+                                     "e2e_frac": round(copy_ms / e2e_ms, 4),
+                                     "note": "the step's host-to-device copies with no attention call: "
+                                             "the host link bounds e2e"}},
         "gpu_launches": LAYERS * args.steps * launches_per_call,
         "step_ms_spread": step_spread,
         "clocks": clk,
