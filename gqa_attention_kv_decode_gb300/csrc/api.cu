@@ -3,6 +3,8 @@
 // runs on the host before anything is launched.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -59,16 +61,25 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   const long lo = tile;
   const long hi = (1024 / tile) * tile;
   if (chunk < lo) chunk = lo;
+  bool one_wave = chunk <= hi;  // else several waves of splits of at most hi rows
   if (chunk > hi) chunk = hi;
   // two tiles or fewer: one CTA per head group is faster than a split plus
   // its merge kernel
   if (max_kv_len <= 2L * tile) chunk = ceil_div(max_kv_len, tile) * tile;
-  if (const int n = g_decode_splits_override.load(std::memory_order_relaxed); n > 0)
+  if (const int n = g_decode_splits_override.load(std::memory_order_relaxed); n > 0) {
     chunk = ceil_div(max_kv_len, n);
+    one_wave = true;  // (so that a request's splits do not depend on the batch)
+  }
   if (chunk < lo) chunk = lo;
   if (ceil_div(max_kv_len, chunk) > 1024) chunk = ceil_div(max_kv_len, 1024);
-  p.chunk = int(chunk);
   p.n_split = int(ceil_div(max_kv_len, chunk));
+  // A request of L keys uses min(n_split, ceil(L / chunk)) splits.  In a
+  // one-wave grid a request shorter than max_kv_len spreads over all of its
+  // splits (at least two tiles each) instead of leaving most of its CTAs
+  // idle while the rest carry full-length chunks; in a grid of several waves
+  // the splits keep at most `hi` rows each, so that long and short requests
+  // balance across the SMs.
+  p.chunk = int(one_wave && p.n_split > 1 ? std::min<long>(chunk, 2L * tile) : chunk);
   return p;
 }
 

@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NREP, R_, NSTAGE>::NTHR, 1)
     }
     return;
   }
-  const int n_used = (L + p.chunk - 1) / p.chunk;
+  // min(n_split, ceil(L / chunk))
+  const int n_used = L > p.chunk * p.n_split ? p.n_split : (L + p.chunk - 1) / p.chunk;
   if (split >= n_used) return;
   // Tiles are dealt round-robin to the request's n_used splits: split s
   // takes tiles s, s + n_used, ...  At any moment the CTAs of one head then

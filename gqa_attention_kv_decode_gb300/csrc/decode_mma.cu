@@ -60,7 +60,8 @@ struct MmaParams {
   unsigned char* v_pool;
   // residual window after a 4-bit cache (len_sub != nullptr): the request
   // attends rows [0, kv_lens[b] - clamp(len_sub[b], 0, max_sub)) of this
-  // cache, and its partial goes to slot ceil(that clamp / slot_chunk)
+  // cache, and its partial goes to slot min(n_slots - 1, ceil(that clamp /
+  // slot_chunk)), the one after the 4-bit splits the request uses
   const int32_t* len_sub;
   int max_sub, slot_chunk;
   int n_slots;        // partial slots per (request, head) row
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
     const int nqc = nq < 0 ? 0 : (nq > p.max_sub ? p.max_sub : nq);
     if ((nqc != nq || L < 0) && split == 0 && blockIdx.y == 0 && tid == 0)
       atomicOr(p.status, GQA_DEV_KVLEN_CLAMPED);
-    slot0 = (nqc + p.slot_chunk - 1) / p.slot_chunk;
+    slot0 = min(p.n_slots - 1, (nqc + p.slot_chunk - 1) / p.slot_chunk);  // the 4-bit splits used
     L = max(L, 0) - nqc;
     if (L < 0) L = 0;
   }
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(MmaCfg<D, NSTAGE, NW>::NTHR, 8 / NW)
     }
     return;
   }
-  const int n_used = (L + p.chunk - 1) / p.chunk;
+  // min(n_split, ceil(L / chunk))
+  const int n_used = L > p.chunk * p.n_split ? p.n_split : (L + p.chunk - 1) / p.chunk;
   if (split >= n_used) return;
   const int nt_all = (L + TILE - 1) / TILE;
   const int nt = (nt_all - split + n_used - 1) / n_used;  // tiles split, split + n_used, ...

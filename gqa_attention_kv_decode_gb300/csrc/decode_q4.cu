@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(Q4Cfg<D, NSTAGE>::NTHR, 4)
     }
     return;
   }
-  const int n_used = (L + p.chunk - 1) / p.chunk;
+  // min(n_split, ceil(L / chunk))
+  const int n_used = L > p.chunk * p.n_split ? p.n_split : (L + p.chunk - 1) / p.chunk;
   if (split >= n_used) return;
   const int nt_all = (L + TILE - 1) / TILE;
   const int nt = (nt_all - split + n_used - 1) / n_used;  // tiles split, split + n_used, ...

@@ -29,11 +29,12 @@ inline WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int n_hc, int n_
   return w;
 }
 
-// The split plan: keys of every request are cut into chunks of `chunk` rows
-// (a multiple of the kernel's tile); chunk s of request b goes to grid x = s.
+// The split plan: a request of L keys uses n_used = min(n_split,
+// ceil(L / chunk)) splits (grid x < n_used), and its tiles are dealt to them
+// round-robin.
 struct SplitPlan {
   int tile;     // rows per shared-memory tile
-  int chunk;    // rows per split
+  int chunk;    // rows per split that count towards n_used
   int n_split;  // grid.x
   int n_hc;     // query-head chunks per KV head (n_rep > 8)
   int nrep_cta; // query heads one CTA serves (<= 8)

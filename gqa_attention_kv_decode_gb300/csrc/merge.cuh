@@ -20,7 +20,8 @@ __device__ __forceinline__ void store_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 // What the merge needs to know about one decode call.  The split kernel
-// writes, for query-head row bh = b*Hq + h and split s < n_used(b),
+// writes, for query-head row bh = b*Hq + h and split s < n_used(b) =
+// min(n_split, ceil(L_b / chunk)),
 // ml[bh*n_split + s] = (max in log2 units, sum) and
 // part_o[(bh*n_split + s)*D + d] = unnormalised output.
 struct MergeParams {
@@ -30,8 +31,9 @@ struct MergeParams {
   const float2* ml;
   const float* part_o;
   // 4-bit cache + residual window (n_quant != nullptr): the 4-bit part of
-  // request b has clamp(n_quant[b], 0, max_quant) keys in chunks of `chunk`,
-  // the window clamp(kv_lens[b] - that, 0, res_cap) keys in one more slot;
+  // request b has clamp(n_quant[b], 0, max_quant) keys in min(n_split - 1,
+  // ceil(that / chunk)) splits, the window clamp(kv_lens[b] - that, 0,
+  // res_cap) keys in one more slot;
   // every used slot holds a partial, even when there is only one.
   const int32_t* n_quant = nullptr;
   int max_quant = 0, res_cap = 0;
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
     nq = nq < 0 ? 0 : (nq > p.max_quant ? p.max_quant : nq);
     int lr = L - nq;
     lr = lr < 0 ? 0 : (lr > p.res_cap ? p.res_cap : lr);
-    n_used = (nq + p.chunk - 1) / p.chunk + (lr > 0 ? 1 : 0);
+    n_used = min(p.n_split - 1, (nq + p.chunk - 1) / p.chunk) + (lr > 0 ? 1 : 0);
     if (n_used == 0) {  // no key at all: zeros
       if (tid == 0) atomicOr(p.status, GQA_DEV_EMPTY_REQUEST);
       if (tid < D4) {
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const MergeParams p) 
     }
   } else {
     L = L < 0 ? 0 : (L > p.max_kv_len ? p.max_kv_len : L);
-    n_used = (L + p.chunk - 1) / p.chunk;
+    n_used = min(p.n_split, (L + p.chunk - 1) / p.chunk);
     if (n_used <= 1) return;  // written by the split kernel itself
   }
 #pragma unroll
