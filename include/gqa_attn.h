@@ -46,6 +46,11 @@
  *     that splits the keys launches two kernels (splits, then merge).
  *   - Arguments are validated on the host before any launch; on failure the
  *     call returns a negative gqa_status_t and launches nothing.
+ *   - The compute entry points may be called from several host threads at
+ *     once, each call with its own outputs and workspace; the settings
+ *     (plan override, wait limit, wait test) are process-wide and change
+ *     only while no other thread is calling.  A calling thread with no
+ *     current CUDA context gets the current device's primary context.
  *   - Per-request lengths that are out of range on the device are clamped
  *     and reported through a status word at the start of the workspace
  *     (GQA_DEV_* bits, OR-accumulated until cleared).
@@ -438,7 +443,9 @@ GQA_ATTN_API int gqa_attn_read_prefill_status(uint32_t* out, void* stream);
 GQA_ATTN_API int gqa_attn_clear_prefill_status(void* stream);
 
 /* Number of splits along the keys the decode entry points use for this
- * problem on the current device (the grid's x extent); exposed for tests. */
+ * problem on the current device (the grid's x extent); exposed for tests.
+ * A request with fewer keys than max_kv_len may use fewer of them; when the
+ * grid is a single wave it spreads its keys over all of them. */
 GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
                                             int dtype);
 
