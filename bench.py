@@ -251,6 +251,52 @@ def sweep_point(binding, S, dtype, device, stream, flush, iters=20, graph=True):
     return res
 
 
+def capacity_points(binding, lens, device, stream, flush, iters=20, cap=32768):
+    """fp32, 7B geometry, 28 layer calls in a CUDA graph on a cache of `cap`
+    rows holding L keys: the call planned for the capacity (max_kv_len = cap,
+    what a graph replayed over many decode steps is captured with) against
+    the call planned for the length itself (max_kv_len = L)."""
+    layers = make_layers(cap, torch.float32, device)
+    outs = [torch.empty_like(q) for q, _, _ in layers]
+    res = []
+    for L in lens:
+        lens_t = torch.tensor([L], dtype=torch.int32, device=device)
+        row = {"L": L, "capacity": cap}
+        for key, mkl in (("planned_for_capacity", cap), ("planned_for_L", L)):
+            ws = binding.decode_workspace(1, HQ, HKV, D, mkl, binding.GQA_F32, device)
+            torch.cuda.synchronize()
+
+            def step():
+                for (q, k, v), o in zip(layers, outs):
+                    binding.gqa_attn_decode(q, k, v, o, lens_t, D ** -0.5, ws, max_kv_len=mkl, stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    step()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            ts = []
+            for _ in range(iters):
+                with torch.cuda.stream(stream):
+                    flush_l2(flush)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3 / LAYERS)
+            us = statistics.median(ts)
+            nbytes = metrics.decode_bytes(HQ, HKV, D, [L], 4)
+            row[key] = {"us_per_call": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+                        "n_split": binding.gqa_attn_decode_num_splits(1, HQ, HKV, D, mkl, binding.GQA_F32)}
+            del g, ws
+        res.append(row)
+    del layers, outs
+    torch.cuda.empty_cache()
+    return res
+
+
 def ragged_point(binding, B, device, stream, flush, iters=10):
     """Hq=32, Hkv=8, D=128, bf16, lengths uniform in [64, 8192], 36 layers."""
     kv_lens = inputs.ragged_kv_lens(B, 64, 8192, seed=inputs.BASE_SEED + B)
@@ -1152,6 +1198,8 @@ def main():
         line["decode_sweep_qwen7b_28_layers"] = sweep
         line["ragged_decode_qwen3_4b_36_layers"] = [ragged_point(binding, B, device, stream, flush)
                                                    for B in (1, 2, 4, 8, 16, 64)]
+        line["capacity_planned_decode_qwen7b_f32_28_layers"] = capacity_points(binding, (512, 2048, 8192), device,
+                                                                               stream, flush)
         line["q4_decode_qwen3_4b_B4_36_layers"] = [q4_point(binding, S, device, stream, flush)
                                                   for S in (64, 2048, 16384)]
         if cpu is not None:  # the oracle beside the GPU figure, same metric
