@@ -53,6 +53,7 @@ EXPORTED = (
     "gqa_attn_read_device_status",
     "gqa_attn_clear_device_status",
     "gqa_attn_decode_num_splits",
+    "gqa_attn_decode_plan_for",
     "gqa_attn_version",
     "gqa_attn_set_plan_override",
     "gqa_attn_set_prefill_interleave_override",
@@ -121,6 +122,9 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_clear_device_status.restype = i32
     L.gqa_attn_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
     L.gqa_attn_decode_num_splits.restype = i32
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    L.gqa_attn_decode_plan_for.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32p, i32p, i32p]
+    L.gqa_attn_decode_plan_for.restype = i32
     L.gqa_attn_version.argtypes = []
     L.gqa_attn_version.restype = i32
     L.gqa_attn_set_plan_override.argtypes = [i32, i32]
@@ -174,6 +178,14 @@ def gqa_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
 
 def gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
     return lib().gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype)
+
+
+def gqa_attn_decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, num_sms):
+    """(n_split, chunk, tile) of the decode plan for a device of num_sms SMs."""
+    n_split, chunk, tile = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().gqa_attn_decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, num_sms, ctypes.byref(n_split),
+                                          ctypes.byref(chunk), ctypes.byref(tile)), "gqa_attn_decode_plan_for")
+    return n_split.value, chunk.value, tile.value
 
 
 def gqa_attn_set_plan_override(decode_splits=0, prefill_kv_split=0) -> None:

@@ -83,10 +83,14 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int max_kv_len, int tile, int num_
   return p;
 }
 
-SplitPlan decode_plan(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype, bool paged) {
+SplitPlan decode_plan_for(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype, bool paged, int num_sms) {
   const long units = long(B) * Hkv * ((Hq / Hkv + 7) / 8);
-  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D, paged, units, max_kv_len),
-                     device_sm_count(), decode_ctas_per_sm(dtype, paged, units, max_kv_len));
+  return plan_splits(B, Hq, Hkv, max_kv_len, decode_tile_rows(dtype, D, paged, units, max_kv_len), num_sms,
+                     decode_ctas_per_sm(dtype, paged, units, max_kv_len));
+}
+
+SplitPlan decode_plan(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype, bool paged) {
+  return decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, paged, device_sm_count());
 }
 
 }  // namespace gqa
@@ -210,6 +214,18 @@ GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int m
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return GQA_ERR_INVALID_ARG;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
   return decode_plan(B, Hq, Hkv, D, max_kv_len, dtype, false).n_split;
+}
+
+GQA_ATTN_API int gqa_attn_decode_plan_for(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype,
+                                          int num_sms, int32_t* n_split, int32_t* chunk, int32_t* tile) {
+  if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return GQA_ERR_INVALID_ARG;
+  if (num_sms < 1 || n_split == nullptr || chunk == nullptr || tile == nullptr) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_UNSUPPORTED;
+  const SplitPlan p = decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, false, num_sms);
+  *n_split = p.n_split;
+  *chunk = p.chunk;
+  *tile = p.tile;
+  return GQA_OK;
 }
 
 GQA_ATTN_API int gqa_attn_decode(const void* q, const void* k, const void* v, void* o,

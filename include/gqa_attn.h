@@ -449,6 +449,17 @@ GQA_ATTN_API int gqa_attn_clear_prefill_status(void* stream);
 GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
                                             int dtype);
 
+/* The split plan gqa_attn_decode would use on a device with num_sms SMs,
+ * computed on the host (no GPU needed; for tests of the planner).  Writes
+ * the grid's split count, the rows per split that count towards a request's
+ * splits, and the kernel's tile height, to host memory: a request of L keys
+ * uses min(n_split, ceil(L / chunk)) splits and deals its tiles to them
+ * round-robin.  GQA_ERR_INVALID_ARG for a shape gqa_attn_decode rejects, a
+ * non-positive num_sms or a null output; GQA_ERR_UNSUPPORTED for a dtype
+ * other than GQA_F32 and GQA_BF16. */
+GQA_ATTN_API int gqa_attn_decode_plan_for(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype,
+                                          int num_sms, int32_t* n_split, int32_t* chunk, int32_t* tile);
+
 /* ABI version (major * 100 + minor). */
 GQA_ATTN_API int gqa_attn_version(void);
 
