@@ -1120,19 +1120,24 @@ def main():
     e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
     e2e_value = replica_value(world, step_bytes, e2e_ms)
     # the same step's host-to-device copies alone: the rate of the host link,
-    # which bounds the end-to-end number (the attention calls hide under it)
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    c0.record(copy_stream)
-    with torch.cuda.stream(copy_stream):
-        for _ in range(e2e_steps):
-            for (hq, hk, hv), (q, k, v) in zip(host, layers):
-                q.copy_(hq, non_blocking=True)
-                k.copy_(hk, non_blocking=True)
-                v.copy_(hv, non_blocking=True)
-    c1.record(copy_stream)
-    torch.cuda.synchronize()
-    copy_ms = dist.max(c0.elapsed_time(c1)) / e2e_steps
+    # which bounds the end-to-end number (the attention calls hide under it).
+    # The faster of two timings: a bound wants the best rate the link gave
+    # (single timings have come out up to 3x slow on a shared host).
+    copy_ms = None
+    for _ in range(2):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(copy_stream)
+        with torch.cuda.stream(copy_stream):
+            for _ in range(e2e_steps):
+                for (hq, hk, hv), (q, k, v) in zip(host, layers):
+                    q.copy_(hq, non_blocking=True)
+                    k.copy_(hk, non_blocking=True)
+                    v.copy_(hv, non_blocking=True)
+        c1.record(copy_stream)
+        torch.cuda.synchronize()
+        t = dist.max(c0.elapsed_time(c1)) / e2e_steps
+        copy_ms = t if copy_ms is None else min(copy_ms, t)
     del host, host_out
 
     traffic = recorded_traffic("decode.cu", "decode_f32_d128_nrep7_S32768")
@@ -1176,7 +1181,7 @@ def main():
                      "n_split": n_split},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-                "h2d_copies_alone": {"ms_per_step": round(copy_ms, 3),
+                "h2d_copies_alone": {"ms_per_step": round(copy_ms, 3), "timings": "faster of 2",
                                      "h2d_gbs": round(h2d / copy_ms / 1e6, 1),
                                      "e2e_frac": round(copy_ms / e2e_ms, 4),
                                      "note": "the step's host-to-device copies with no attention call: "
