@@ -3,7 +3,7 @@
 Mistakes are planted in the oracle's own computation, at the headline decode
 geometry (Qwen2.5-7B heads, one KV head group, 32,768 keys): a split of the
 keys left out, and a log-sum-exp merge that forgets the per-split maxima.
-Each planted result passes the benchmark spec's absolute 2e-2 bound, which is why the
+Each planted result passes the bf16 absolute bound of 2e-2, which is why the
 scaled bound exists, and fails the scaled bound.  A bf16-rounded copy of the
 true result passes both.
 """
