@@ -123,7 +123,7 @@ def lib() -> ctypes.CDLL:
     L.gqa_attn_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
     L.gqa_attn_decode_num_splits.restype = i32
     i32p = ctypes.POINTER(ctypes.c_int32)
-    L.gqa_attn_decode_plan_for.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32p, i32p, i32p]
+    L.gqa_attn_decode_plan_for.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32p, i32p, i32p]
     L.gqa_attn_decode_plan_for.restype = i32
     L.gqa_attn_version.argtypes = []
     L.gqa_attn_version.restype = i32
@@ -180,11 +180,15 @@ def gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype) -> int:
     return lib().gqa_attn_decode_num_splits(B, Hq, Hkv, D, max_kv_len, dtype)
 
 
-def gqa_attn_decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, num_sms):
-    """(n_split, chunk, tile) of the decode plan for a device of num_sms SMs."""
+GQA_PLAN_DECODE, GQA_PLAN_PAGED, GQA_PLAN_Q4 = 0, 1, 2
+
+
+def gqa_attn_decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, num_sms, variant=GQA_PLAN_DECODE):
+    """(n_split, chunk, tile) of a decode plan for a device of num_sms SMs."""
     n_split, chunk, tile = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-    _check(lib().gqa_attn_decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, num_sms, ctypes.byref(n_split),
-                                          ctypes.byref(chunk), ctypes.byref(tile)), "gqa_attn_decode_plan_for")
+    rc = lib().gqa_attn_decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, variant, num_sms, ctypes.byref(n_split),
+                                        ctypes.byref(chunk), ctypes.byref(tile))
+    _check(rc, "gqa_attn_decode_plan_for")
     return n_split.value, chunk.value, tile.value
 
 

@@ -217,11 +217,17 @@ GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int m
 }
 
 GQA_ATTN_API int gqa_attn_decode_plan_for(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype,
-                                          int num_sms, int32_t* n_split, int32_t* chunk, int32_t* tile) {
+                                          int variant, int num_sms, int32_t* n_split, int32_t* chunk,
+                                          int32_t* tile) {
   if (check_decode_shape(B, Hq, Hkv, D, max_kv_len, max_kv_len, 1.f) != GQA_OK) return GQA_ERR_INVALID_ARG;
   if (num_sms < 1 || n_split == nullptr || chunk == nullptr || tile == nullptr) return GQA_ERR_INVALID_ARG;
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_UNSUPPORTED;
-  const SplitPlan p = decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, false, num_sms);
+  if (variant < GQA_PLAN_DECODE || variant > GQA_PLAN_Q4) return GQA_ERR_INVALID_ARG;
+  if (variant == GQA_PLAN_Q4 ? dtype != GQA_BF16 : (dtype != GQA_F32 && dtype != GQA_BF16))
+    return GQA_ERR_UNSUPPORTED;
+  const SplitPlan p =
+      variant == GQA_PLAN_Q4
+          ? plan_splits(B, Hq, Hkv, max_kv_len, decode_q4_tile_rows(D), num_sms, decode_q4_ctas_per_sm())
+          : decode_plan_for(B, Hq, Hkv, D, max_kv_len, dtype, variant == GQA_PLAN_PAGED, num_sms);
   *n_split = p.n_split;
   *chunk = p.chunk;
   *tile = p.tile;

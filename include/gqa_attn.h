@@ -449,16 +449,24 @@ GQA_ATTN_API int gqa_attn_clear_prefill_status(void* stream);
 GQA_ATTN_API int gqa_attn_decode_num_splits(int B, int Hq, int Hkv, int D, int max_kv_len,
                                             int dtype);
 
-/* The split plan gqa_attn_decode would use on a device with num_sms SMs,
- * computed on the host (no GPU needed; for tests of the planner).  Writes
- * the grid's split count, the rows per split that count towards a request's
- * splits, and the kernel's tile height, to host memory: a request of L keys
- * uses min(n_split, ceil(L / chunk)) splits and deals its tiles to them
- * round-robin.  GQA_ERR_INVALID_ARG for a shape gqa_attn_decode rejects, a
- * non-positive num_sms or a null output; GQA_ERR_UNSUPPORTED for a dtype
- * other than GQA_F32 and GQA_BF16. */
+/* Which decode kernel a plan is for (gqa_attn_decode_plan_for). */
+typedef enum gqa_plan_variant {
+  GQA_PLAN_DECODE = 0, /* gqa_attn_decode (contiguous cache), dtype GQA_F32 or GQA_BF16  */
+  GQA_PLAN_PAGED = 1,  /* gqa_attn_decode_paged, dtype GQA_F32 or GQA_BF16             */
+  GQA_PLAN_Q4 = 2      /* gqa_attn_decode_q4 (4-bit cache; bf16 queries), dtype GQA_BF16 */
+} gqa_plan_variant_t;
+
+/* The split plan the decode kernel of `variant` would use on a device with
+ * num_sms SMs, computed on the host (no GPU needed; for tests of the
+ * planner).  Writes the grid's split count, the rows per split that count
+ * towards a request's splits, and the kernel's tile height, to host memory:
+ * a request of L keys uses min(n_split, ceil(L / chunk)) splits and deals
+ * its tiles to them round-robin.  GQA_ERR_INVALID_ARG for a shape the decode
+ * entry points reject, an unknown variant, a non-positive num_sms or a null
+ * output; GQA_ERR_UNSUPPORTED for a dtype the variant has no kernel for. */
 GQA_ATTN_API int gqa_attn_decode_plan_for(int B, int Hq, int Hkv, int D, int max_kv_len, int dtype,
-                                          int num_sms, int32_t* n_split, int32_t* chunk, int32_t* tile);
+                                          int variant, int num_sms, int32_t* n_split, int32_t* chunk,
+                                          int32_t* tile);
 
 /* ABI version (major * 100 + minor). */
 GQA_ATTN_API int gqa_attn_version(void);

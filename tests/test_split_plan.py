@@ -1,5 +1,7 @@
-"""The decode split planner, on the host (no GPU): the plan for a device of a
-given SM count, checked against the rule the kernels and the merge follow.
+"""The decode split planner, on the host (no GPU): the plans of the fp32 and
+bf16 kernels (contiguous and paged caches) and of the 4-bit kernel for a
+device of a given SM count, checked against the rule the kernels and the
+merge follow.
 
 A request of L keys uses n_used(L) = min(n_split, ceil(L / chunk)) splits
 and deals its ceil(L / tile) tiles to them round-robin.  The properties:
@@ -16,12 +18,15 @@ import pytest
 
 from gqa_attention_kv_decode_gb300 import binding
 
-SHAPES = [(B, Hq, Hkv, D, S, dt)
+KERNELS = [(binding.GQA_PLAN_DECODE, binding.GQA_F32), (binding.GQA_PLAN_DECODE, binding.GQA_BF16),
+           (binding.GQA_PLAN_PAGED, binding.GQA_F32), (binding.GQA_PLAN_PAGED, binding.GQA_BF16),
+           (binding.GQA_PLAN_Q4, binding.GQA_BF16)]
+SHAPES = [(B, Hq, Hkv, D, S, variant, dt)
           for B in (1, 2, 4, 16, 64)
           for Hq, Hkv in ((28, 4), (32, 8), (14, 2))
           for D in (64, 128)
           for S in (64, 128, 2048, 8192, 32768)
-          for dt in (binding.GQA_F32, binding.GQA_BF16)]
+          for variant, dt in KERNELS]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,10 +43,10 @@ def lengths(S):
     return sorted({1, 2, S // 3, S // 2, max(1, S - 1), S} | set(range(1, min(S, 300) + 1, 7)))
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,D,S,dt", SHAPES)
-def test_plan_invariants(B, Hq, Hkv, D, S, dt):
-    n_split, chunk, tile = binding.gqa_attn_decode_plan_for(B, Hq, Hkv, D, S, dt, 152)
-    assert 1 <= n_split <= 1024 and tile in (32, 64, 128) and chunk >= 1
+@pytest.mark.parametrize("B,Hq,Hkv,D,S,variant,dt", SHAPES)
+def test_plan_invariants(B, Hq, Hkv, D, S, variant, dt):
+    n_split, chunk, tile = binding.gqa_attn_decode_plan_for(B, Hq, Hkv, D, S, dt, 152, variant)
+    assert 1 <= n_split <= 1024 and tile in (16, 32, 64, 128) and chunk >= 1
     assert n_used(S, n_split, chunk) == n_split, "a full-length request uses every planned split"
     prev = 0
     for L in lengths(S):
@@ -97,3 +102,12 @@ def test_plan_for_rejects(args, status):
     with pytest.raises(binding.GqaAttnError) as e:
         binding.gqa_attn_decode_plan_for(*args[:5], binding.GQA_F32 if args[5] == 0 else args[5], args[6])
     assert e.value.status == status
+
+
+def test_plan_for_rejects_unknown_variants_and_fp32_queries_for_q4():
+    with pytest.raises(binding.GqaAttnError) as e:
+        binding.gqa_attn_decode_plan_for(1, 32, 8, 128, 100, binding.GQA_BF16, 152, 3)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    with pytest.raises(binding.GqaAttnError) as e:
+        binding.gqa_attn_decode_plan_for(1, 32, 8, 128, 100, binding.GQA_F32, 152, binding.GQA_PLAN_Q4)
+    assert e.value.status == binding.GQA_ERR_UNSUPPORTED
